@@ -1,0 +1,195 @@
+"""ctypes binding for ``libattn_b300.so`` (argument marshalling only).
+
+Every entry point here checks that the torch tensors it is handed have the
+dtype, device and contiguity the C ABI expects, then passes raw device
+pointers, sizes and the current CUDA stream to the library.  All arithmetic
+runs in the library's kernels; there is no fallback of any kind.  If the
+library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+# Status codes of include/attn_b300.h
+ATTN_OK = 0
+ATTN_EINVAL = 1
+ATTN_EUNSUPPORTED = 2
+ATTN_ECUDA = 3
+ATTN_EDEVICE = 4
+_STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_EINVAL", 2: "ATTN_EUNSUPPORTED",
+                 3: "ATTN_ECUDA", 4: "ATTN_EDEVICE"}
+
+# Every symbol the header declares, with (restype, argtypes).
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+SIGNATURES = {
+    "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "paged_decode_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "paged_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
+                          _vp, _vp, _vp, _sz, _vp]),
+    "attn_last_error": (ctypes.c_char_p, []),
+    "attn_device_status": (_i, [_vp]),
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libattn_b300.so")
+
+
+def load_library():
+    """Load the CUDA library (once).  Raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m attention_fa_attn_fwd_b300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def _check(status: int):
+    if status != ATTN_OK:
+        msg = load_library().attn_last_error()
+        raise AttnError(status, msg.decode() if msg else "")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+             causal: bool = False, scale: Optional[float] = None,
+             o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+             want_lse: bool = True, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """O = softmax(scale Q K^T [causal]) V and per-row LSE via ``attn_fwd``.
+
+    q [B,H,Nq,d], k/v [B,Hkv,Nk,d], bf16, contiguous, on one CUDA device.
+    Returns (o [B,H,Nq,d] bf16, lse [B,H,Nq] fp32 or None).
+    """
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k, "k", torch.bfloat16, 4)
+    _need(v, "v", torch.bfloat16, 4)
+    B, H, Nq, d = q.shape
+    _, Hkv, Nk, _ = k.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _need(o, "o", torch.bfloat16, 4)
+        if o.shape != q.shape:
+            raise ValueError("o must have q's shape")
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+        if tuple(lse.shape) != (B, H, Nq):
+            raise ValueError("lse must be [B, H, Nq]")
+    st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                      lse.data_ptr() if lse is not None else None,
+                      B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                      _stream_handle(stream))
+    _check(st)
+    return o, lse
+
+
+def paged_decode_workspace_size(num_seqs: int, H: int, d: int, max_blocks_per_seq: int,
+                                block_size: int = 16) -> int:
+    return int(load_library().paged_decode_workspace_size(num_seqs, H, d, max_blocks_per_seq,
+                                                          block_size))
+
+
+def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 block_table: torch.Tensor, seq_lens: torch.Tensor,
+                 scale: Optional[float] = None, o: Optional[torch.Tensor] = None,
+                 lse: Optional[torch.Tensor] = None, want_lse: bool = True,
+                 workspace: Optional[torch.Tensor] = None,
+                 stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Decode attention over a paged KV cache via ``paged_decode``.
+
+    q [S,H,d] bf16; k_cache/v_cache [num_blocks,Hkv,block_size,d] bf16;
+    block_table [S,max_blocks] int32; seq_lens [S] int32.  ``workspace`` is a
+    uint8 CUDA tensor of at least ``paged_decode_workspace_size`` bytes
+    (allocated here if omitted).  Returns (o [S,H,d] bf16, lse [S,H] fp32).
+    """
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    S, H, d = q.shape
+    num_blocks, Hkv, block_size, dk = k_cache.shape
+    if v_cache.shape != k_cache.shape or dk != d:
+        raise ValueError("k_cache / v_cache / q shapes disagree")
+    if block_table.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_table / seq_lens must have num_seqs rows")
+    max_blocks = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _need(o, "o", torch.bfloat16, 3)
+    if lse is None and want_lse:
+        lse = torch.empty((S, H), dtype=torch.float32, device=q.device)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    ws_bytes = paged_decode_workspace_size(S, H, d, max_blocks, block_size)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    elif workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise TypeError("workspace must be a uint8 CUDA tensor")
+    st = lib.paged_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                          block_table.data_ptr(), seq_lens.data_ptr(),
+                          S, H, Hkv, d, num_blocks, max_blocks, block_size, float(scale),
+                          o.data_ptr(), lse.data_ptr() if lse is not None else None,
+                          workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    _check(st)
+    return o, lse
+
+
+def device_status(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the kernels' device error word."""
+    return int(load_library().attn_device_status(_stream_handle(stream)))
