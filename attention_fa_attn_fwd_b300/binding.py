@@ -134,10 +134,9 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     return o, lse
 
 
-def paged_decode_workspace_size(num_seqs: int, H: int, d: int, max_blocks_per_seq: int,
-                                block_size: int = 16) -> int:
-    return int(load_library().paged_decode_workspace_size(num_seqs, H, d, max_blocks_per_seq,
-                                                          block_size))
+def paged_decode_workspace_size(num_seqs: int, H: int, Hkv: int, d: int,
+                                max_blocks_per_seq: int) -> int:
+    return int(load_library().paged_decode_workspace_size(num_seqs, H, Hkv, d, max_blocks_per_seq))
 
 
 def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -176,7 +175,7 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         lse = torch.empty((S, H), dtype=torch.float32, device=q.device)
     elif lse is not None:
         _need(lse, "lse", torch.float32, 2)
-    ws_bytes = paged_decode_workspace_size(S, H, d, max_blocks, block_size)
+    ws_bytes = paged_decode_workspace_size(S, H, Hkv, d, max_blocks)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     elif workspace.dtype != torch.uint8 or not workspace.is_cuda:

@@ -1,0 +1,37 @@
+// Internal declarations shared by the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+// Encodes a tiled TMA descriptor; returns false on failure (message in err).
+bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128,
+                      const char** err);
+
+// ---- prefill (prefill_sm103.cu)
+int prefill_smem_bytes(int d);
+cudaError_t prefill_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                           int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                           cudaStream_t stream, const char** err);
+int prefill_take_device_error();  // reads and clears (synchronous)
+
+// ---- paged decode (decode_sm103.cu)
+struct DecodePlan {
+  int blocks_per_split;
+  int max_splits;
+  size_t workspace_bytes;
+};
+DecodePlan decode_plan(int num_seqs, int H, int Hkv, int d, int max_blocks_per_seq);
+cudaError_t decode_launch(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_table, const int32_t* seq_lens, int num_seqs, int H,
+                          int Hkv, int d, int num_blocks, int max_blocks_per_seq, float scale,
+                          void* o, float* lse, void* workspace, const DecodePlan& plan,
+                          cudaStream_t stream, const char** err);
+int decode_take_device_error();
+
+}  // namespace attn

@@ -1,0 +1,443 @@
+"""Benchmark of the attention hot path on B300: prints ONE JSON line.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+  * prefill: attn_fwd on the long-context causal GQA workload
+    (B=1, H=32, Hkv=8, Nq=Nk=16384, d=128, Q,K ~ N(0,1)*1.5, V ~ N(0,1));
+  * decode:  paged_decode on 64 sequences x 1 query token, H=32, Hkv=8,
+    d=128, lengths U{1024..8192}, block 16, groups of 4 sharing a 512-token
+    prefix, permuted NaN-poisoned pool.
+``value`` is the prefill throughput in TFLOP/s (FLOPs = 4*B*H*Nq*Nk*d, halved
+for causal); the decode throughput (KV GB/s over the unique bytes read) is
+reported beside it.  Kernel times are CUDA events on the launching stream,
+with a 256 MiB L2 flush (outside the events) before every kernel.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same step on its own GPU
+(independent replicas: weak scaling); times are the max over ranks.
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+workload (the reference arm of this benchmark).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from attention_fa_attn_fwd_b300 import workloads  # noqa: E402
+
+PREFILL = "gqa_b1h32kv8_n16384_d128_causal"
+DECODE = "paged_decode_s64_h32kv8_d128"
+METRIC = "prefill attn TFLOP/s & % BF16 tensor peak; paged decode KV GB/s & % HBM"
+FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p["bf16_tflops_sustained"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "source": "fallback"}
+
+
+def prefill_flops(cfg) -> float:
+    f = 4.0 * cfg["B"] * cfg["H"] * cfg["Nq"] * cfg["Nk"] * cfg["d"]
+    return f / 2 if cfg["causal"] else f
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "attention_fa_attn_fwd_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, files):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since it was captured; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            t = json.load(fh)[kernel]
+        if t.get("source_sha256") == source_hash(files):
+            return float(t["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = [r for (t, r) in self.samples if t0 <= t <= t1 + 0.05]
+        if not rows:
+            rows = [r for (_, r) in self.samples[-3:]]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if len(r) > 6 + i and r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_prefill_sample(q, k, v, cfg, budget_s: float, seed: int = 0):
+    """Time the fp64 oracle on seeded query rows of the prefill workload until
+    ~budget_s of CPU work; returns (TFLOP/s, description, flops, seconds)."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+    f = lambda t: oracle.bf16_bits_to_f64(t.contiguous().view(torch.int16).numpy())
+    scale = 1.0 / math.sqrt(cfg["d"])
+    G = cfg["H"] // cfg["Hkv"]
+    flops = 0.0
+    rows_done = 0
+    t_total = 0.0
+    t_start = time.perf_counter()
+    while time.perf_counter() - t_start < budget_s:
+        h = int(rng.integers(cfg["H"]))
+        rows = np.sort(rng.choice(cfg["Nq"], size=16, replace=False))
+        qh = f(q[:, h:h + 1])
+        kh = f(k[:, h // G:h // G + 1])
+        vh = f(v[:, h // G:h // G + 1])
+        t0 = time.perf_counter()
+        oracle.attention_ref(qh, kh, vh, scale, cfg["causal"], rows=rows)
+        t_total += time.perf_counter() - t0
+        for i in rows:
+            keys = (min(cfg["Nk"], i + 1 + cfg["Nk"] - cfg["Nq"]) if cfg["causal"] else cfg["Nk"])
+            flops += 4.0 * cfg["d"] * keys
+        rows_done += len(rows)
+    desc = f"{rows_done} seeded query rows (16 per sampled head) of {PREFILL}"
+    return flops / t_total / 1e12, desc, flops, t_total
+
+
+def oracle_decode_sample(pb, budget_s: float):
+    import numpy as np
+    import oracle
+    f = lambda t: oracle.bf16_bits_to_f64(t.contiguous().view(torch.int16).numpy())
+    scale = 1.0 / math.sqrt(pb.q.shape[-1])
+    nbytes = 0
+    t_total = 0.0
+    n = 0
+    t_start = time.perf_counter()
+    per_tok = pb.k_cache.shape[1] * pb.k_cache.shape[3] * 2 * 2
+    while time.perf_counter() - t_start < budget_s and n < pb.num_seqs:
+        k, v = pb.logical_kv(n)
+        kk, vv, qq = f(k), f(v), f(pb.q[n:n + 1])
+        t0 = time.perf_counter()
+        oracle.paged_decode_ref(qq, [kk], [vv], scale)
+        t_total += time.perf_counter() - t0
+        nbytes += int(pb.seq_lens[n]) * per_tok
+        n += 1
+    return nbytes / t_total / 1e9, f"{n} of {pb.num_seqs} sequences of {DECODE}", t_total
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        n = max((i.get("num_threads", 1) for i in info if i.get("user_api") == "blas"), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, ws, rank):
+    """Reference arm: the fp64 CPU oracle, bounded sample per step."""
+    if rank != 0:
+        return
+    cfg = workloads.PREFILL_WORKLOADS[PREFILL]
+    q, k, v = workloads.prefill_inputs(**cfg, seed=0)
+    pb = workloads.paged_decode_inputs(**workloads.PAGED_WORKLOADS[DECODE], seed=0)
+    per_step = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_prefill_sample(q, k, v, cfg, per_step * 0.2)
+    vals, dec, secs = [], [], []
+    for i in range(args.steps):
+        tf, desc, _, t = oracle_prefill_sample(q, k, v, cfg, per_step * 0.8, seed=i + 1)
+        gbs, ddesc, td = oracle_decode_sample(pb, per_step * 0.2)
+        vals.append(tf)
+        dec.append(gbs)
+        secs.append(t + td)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{PREFILL} + {DECODE}", "prefill": cfg,
+                   "decode": workloads.PAGED_WORKLOADS[DECODE], "l2": "n/a (CPU)"},
+        "decode": {"value": statistics.median(dec), "unit": "GB/s"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
+                         "kind": "oracle", "sample": f"per step: {desc}; decode {ddesc}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ws, rank, local):
+    from attention_fa_attn_fwd_b300 import binding
+    binding.load_library()  # fails loudly if the CUDA library is missing
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    cfg = workloads.PREFILL_WORKLOADS[PREFILL]
+    dcfg = workloads.PAGED_WORKLOADS[DECODE]
+    q_h, k_h, v_h = workloads.prefill_inputs(**cfg, seed=rank)
+    pb = workloads.paged_decode_inputs(**dcfg, seed=rank)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(cfg["B"], cfg["H"], cfg["Nq"], dtype=torch.float32, device=dev)
+    dq, kc, vc = pb.q.to(dev), pb.k_cache.to(dev), pb.v_cache.to(dev)
+    bt, sl = pb.block_table.to(dev), pb.seq_lens.to(dev)
+    do = torch.empty_like(dq)
+    dlse = torch.empty(dq.shape[0], dq.shape[1], dtype=torch.float32, device=dev)
+    wsb = binding.paged_decode_workspace_size(dq.shape[0], dq.shape[1], kc.shape[1], dq.shape[2],
+                                              bt.shape[1])
+    wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill():
+        binding.attn_fwd(q, k, v, causal=True, o=o, lse=lse, stream=stream)
+
+    def decode():
+        binding.paged_decode(dq, kc, vc, bt, sl, o=do, lse=dlse, workspace=wsp, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        prefill()
+        flush.zero_()
+        decode()
+    torch.cuda.synchronize()
+    assert binding.device_status(stream) == 0
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.6)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        evs[i][0].record(stream)
+        prefill()
+        evs[i][1].record(stream)
+        flush.zero_()
+        evs[i][2].record(stream)
+        decode()
+        evs[i][3].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    launches = 3 * K
+    p_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]
+    d_ms = [evs[i][2].elapsed_time(evs[i][3]) for i in range(K)]
+    p_mean = max_over_ranks(statistics.mean(p_ms), ws)
+    d_mean = max_over_ranks(statistics.mean(d_ms), ws)
+    assert binding.device_status(stream) == 0
+
+    flops = prefill_flops(cfg)
+    tflops = flops / (p_mean * 1e-3) / 1e12
+    per_tok = kc.shape[1] * kc.shape[3] * 2 * 2
+    uniq_bytes = pb.unique_valid_tokens() * per_tok
+    logical_bytes = pb.logical_tokens() * per_tok
+    small_bytes = (dq.numel() * 2 * 2 + bt.numel() * 4 + sl.numel() * 4 + dlse.numel() * 4)
+    dec_gbs = (uniq_bytes + small_bytes) / (d_mean * 1e-3) / 1e9
+
+    # ---- end to end through the public API with pinned host buffers
+    qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+    op = torch.empty(q_h.shape, dtype=torch.bfloat16).pin_memory()
+    lp = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    dqp, btp, slp = pb.q.pin_memory(), pb.block_table.pin_memory(), pb.seq_lens.pin_memory()
+    dop = torch.empty(pb.q.shape, dtype=torch.bfloat16).pin_memory()
+    dlp = torch.empty(dlse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (qp, kp, vp, dqp, btp, slp))
+    d2h = sum(t.numel() * t.element_size() for t in (op, lp, dop, dlp))
+    Ke = max(3, min(K, 10))
+    e_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(Ke)]
+
+    def e2e_step(ev):
+        flush.zero_()
+        if ev:
+            ev[0].record(stream)
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        prefill()
+        op.copy_(o, non_blocking=True)
+        lp.copy_(lse, non_blocking=True)
+        if ev:
+            ev[1].record(stream)
+        dq.copy_(dqp, non_blocking=True)
+        bt.copy_(btp, non_blocking=True)
+        sl.copy_(slp, non_blocking=True)
+        decode()
+        dop.copy_(do, non_blocking=True)
+        dlp.copy_(dlse, non_blocking=True)
+        if ev:
+            ev[2].record(stream)
+
+    e2e_step(None)  # untimed warm-up
+    for i in range(Ke):
+        e2e_step(e_evs[i])
+    torch.cuda.synchronize()
+    ep = max_over_ranks(statistics.mean(e_evs[i][0].elapsed_time(e_evs[i][1]) for i in range(Ke)), ws)
+    ed = max_over_ranks(statistics.mean(e_evs[i][1].elapsed_time(e_evs[i][2]) for i in range(Ke)), ws)
+    e2e_tflops = flops / (ep * 1e-3) / 1e12
+
+    if rank != 0:
+        return
+    clocks = sampler.summary(t0, t1)
+    traffic = committed_traffic("prefill_fwd_kernel", ["prefill_sm103.cu", "ptx.cuh"])
+    cpu_tf, cpu_desc, _, _ = oracle_prefill_sample(q_h, k_h, v_h, cfg, args.cpu_budget)
+    cpu_dec, cpu_ddesc, _ = oracle_decode_sample(pb, max(1.0, args.cpu_budget / 4))
+    peak_tf = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": p_mean + d_mean, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{PREFILL} + {DECODE}", "prefill": cfg, "decode": dcfg,
+                   "l2": "256 MiB L2 flush before every kernel (outside the events)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "prefill": {"ms": p_mean, "tflops": tflops, "frac_burst": tflops / peak_tf,
+                    "frac_sustained": tflops / peaks["bf16_tflops_sustained"]},
+        "decode": {"ms": d_mean, "value": dec_gbs, "unit": "GB/s",
+                   "unique_kv_bytes": uniq_bytes, "logical_kv_bytes": logical_bytes,
+                   "logical_gbs": (logical_bytes + small_bytes) / (d_mean * 1e-3) / 1e9,
+                   "frac_hbm_measured": dec_gbs / peaks["hbm_gbs"], "frac_hbm_8tbs": dec_gbs / 8000.0},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": tflops / peak_tf, "traffic": traffic,
+                     "kernel": "prefill_fwd_kernel<128>", "peak_kind": f"bf16 burst ({peaks['source']})"},
+        "roofline_decode": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
+                            "traffic": committed_traffic("decode_split_kernel", ["decode_sm103.cu", "ptx.cuh"]),
+                            "kernel": "decode_split_kernel<128> + decode_merge_kernel<128>"},
+        "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "prefill_ms": ep, "decode_ms": ed,
+                "decode_gbs": (uniq_bytes + small_bytes) / (ed * 1e-3) / 1e9},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": blas_threads(),
+                         "kind": "oracle", "sample": cpu_desc,
+                         "decode_gbs": cpu_dec, "decode_sample": cpu_ddesc},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of CPU oracle work for the cpu_baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,143 @@
+/*
+ * attn_b300.h -- C ABI of libattn_b300.so: exact attention forward
+ * (FlashAttention-2-style prefill) and paged-KV decode for NVIDIA B300
+ * (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers to tensors are DEVICE pointers on the current CUDA device,
+ *   allocated and owned by the caller; the library never frees or retains
+ *   them.  The library allocates no device memory in these calls.
+ * - Element types: q, k, v, o, k_cache, v_cache are bfloat16 (passed as
+ *   void*), lse is float32, block_table and seq_lens are int32.
+ * - Every tensor is dense and contiguous in the layout stated per call.
+ * - Calls are asynchronous on `stream` (NULL = legacy default stream) and
+ *   never synchronise.  Results are deterministic: identical calls give
+ *   bit-identical outputs.
+ * - Errors: on invalid arguments nothing is launched and a non-zero status is
+ *   returned; attn_last_error() then returns a human-readable message (per
+ *   calling thread).  Kernels bound every internal wait; a wait that times
+ *   out records a code read by attn_device_status().
+ *
+ * Notation (source pages): Interview notes "他人面经整理", answer
+ * "介绍你理解的flashattention", part 1 defines self-attention as
+ * Softmax(Q K^T / sqrt(d_k)) V; part 2 gives the tiled single-pass online
+ * softmax.  Tutorial "第 3 章 进阶原理:性能模型与数值稳定性", sections
+ * 3.0.6-3.0.7, gives PagedAttention: KV blocks of 16 tokens behind a block
+ * table, physical blocks shared by sequences with a common prefix.
+ */
+#ifndef ATTN_B300_H_
+#define ATTN_B300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+/* Compatible with cudaStream_t (struct CUstream_st*). */
+typedef struct CUstream_st* attn_stream_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_EINVAL = 1,       /* bad argument: null pointer, bad size, misaligned, ... */
+  ATTN_EUNSUPPORTED = 2, /* valid but not implemented here (head dim, GQA ratio, GPU) */
+  ATTN_ECUDA = 3,        /* a CUDA runtime call or launch failed */
+  ATTN_EDEVICE = 4       /* a kernel recorded a device-side error (attn_device_status) */
+} attn_status;
+
+/*
+ * attn_fwd -- O = softmax(scale * Q K^T [+ causal mask]) V, plus per-row LSE.
+ *
+ * Defined by: interview notes "他人面经整理", flashattention answer, part 1
+ * (the formula) and part 2 (tiling + online softmax: S and P are never
+ * written to device memory).
+ *
+ *   q    [B, H,   Nq, d]  bf16, contiguous (row-major, d fastest)
+ *   k    [B, Hkv, Nk, d]  bf16, contiguous
+ *   v    [B, Hkv, Nk, d]  bf16, contiguous
+ *   o    [B, H,   Nq, d]  bf16 output
+ *   lse  [B, H,   Nq]     fp32 output, or NULL to skip.
+ *        lse[i] = ln sum_j exp(scale * q_i . k_j) over the unmasked keys
+ *        (natural log); -inf (and o row = 0) for a row with no unmasked key.
+ *   scale  > 0 and finite (the definition uses 1/sqrt(d)).
+ *   causal 0: every key; 1: bottom-right aligned mask, query row i attends
+ *          key j iff j <= i + (Nk - Nq).
+ *   GQA: query head h reads key/value head h / (H / Hkv).
+ *
+ * Requirements: B, H, Hkv, Nq, Nk >= 1; H % Hkv == 0; d in {64, 128}
+ * (else ATTN_EUNSUPPORTED); every pointer 16-byte aligned; the device is
+ * sm_103 (else ATTN_EUNSUPPORTED).  B*H*ceil(Nq/128) < 2^31.
+ */
+ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                     attn_stream_t stream);
+
+/*
+ * paged_decode_workspace_size -- bytes of device workspace paged_decode needs
+ * for these sizes (it holds the per-split partial results merged by LSE).
+ * Returns 0 for invalid sizes.  Pure host function.
+ */
+ATTN_API size_t paged_decode_workspace_size(int num_seqs, int H, int Hkv, int d, int max_blocks_per_seq);
+
+/*
+ * paged_decode -- one query token per sequence attends all seq_lens[s] cached
+ * keys of its sequence, read through a block table (no causal mask: every
+ * cached key precedes the new token).
+ *
+ * Defined by: tutorial "第 3 章 进阶原理:性能模型与数值稳定性", sections
+ * 3.0.6-3.0.7 (PagedAttention block table, block size 16, shared prefix
+ * blocks), and the same definition as attn_fwd with Nq = 1.
+ *
+ *   q            [num_seqs, H, d]                      bf16
+ *   k_cache      [num_blocks, Hkv, block_size, d]      bf16 (pool of physical blocks)
+ *   v_cache      [num_blocks, Hkv, block_size, d]      bf16
+ *   block_table  [num_seqs, max_blocks_per_seq]        int32; entry [s][i] is the
+ *                physical block holding tokens 16i .. 16i+15 of sequence s.
+ *                Entries past ceil(seq_lens[s]/16) are never read.  Several
+ *                sequences may map the same physical block (shared prefix).
+ *   seq_lens     [num_seqs]                            int32, 0 <= len <= 16*max_blocks_per_seq
+ *   o            [num_seqs, H, d]                      bf16 output
+ *   lse          [num_seqs, H]                         fp32 output or NULL
+ *   workspace    device scratch of >= paged_decode_workspace_size(...) bytes,
+ *                16-byte aligned, owned by the caller; contents need no
+ *                initialisation and are clobbered.
+ *
+ * Cache slots past a sequence's length may hold any bits (even NaN); they do
+ * not affect the result.  A block_table entry outside [0, num_blocks) is
+ * read as zeros and recorded as a device error (attn_device_status).
+ * A sequence of length 0 gets o = 0 and lse = -inf.
+ *
+ * Requirements: block_size == 16; H % Hkv == 0 and H / Hkv <= 8; d in
+ * {64, 128}; num_blocks * Hkv * 16 < 2^31; pointers 16-byte aligned
+ * (block_table, seq_lens and lse: 4-byte aligned).
+ */
+ATTN_API attn_status paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_table, const int32_t* seq_lens, int num_seqs, int H,
+                         int Hkv, int d, int num_blocks, int max_blocks_per_seq, int block_size,
+                         float scale, void* o, float* lse, void* workspace,
+                         size_t workspace_bytes, attn_stream_t stream);
+
+/* Message for the last non-OK status returned on the calling thread. */
+ATTN_API const char* attn_last_error(void);
+
+/*
+ * attn_device_status -- synchronises `stream`, then reads and clears the
+ * device error words the kernels set (a bounded wait that timed out, an
+ * out-of-range block id).  Returns ATTN_OK, ATTN_EDEVICE (message holds the
+ * code) or ATTN_ECUDA.  A debugging aid, not needed for normal operation.
+ */
+ATTN_API attn_status attn_device_status(attn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_B300_H_ */

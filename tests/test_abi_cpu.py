@@ -1,0 +1,112 @@
+"""The C-ABI library loads without a GPU, exports every declared symbol, and
+rejects invalid arguments before touching the device (CPU only)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_fa_attn_fwd_b300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_b300.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"ATTN_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_fa_attn_fwd_b300 import build
+    build.build()
+    return binding.load_library()
+
+
+def test_header_declares_expected_api():
+    assert declared_functions() == sorted(["attn_fwd", "paged_decode", "paged_decode_workspace_size",
+                                           "attn_last_error", "attn_device_status"])
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(binding.SIGNATURES)
+
+
+def _fake(n=0):
+    return ctypes.c_void_p(0x10000 + 256 * n)  # aligned, never dereferenced
+
+
+def _fwd(lib, **kw):
+    a = dict(q=_fake(1), k=_fake(2), v=_fake(3), o=_fake(4), lse=None, B=1, H=2, Hkv=2, Nq=128,
+             Nk=128, d=64, scale=0.125, causal=0, stream=None)
+    a.update(kw)
+    return lib.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Hkv"],
+                        a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), binding.ATTN_EINVAL),
+    (dict(o=None), binding.ATTN_EINVAL),
+    (dict(B=0), binding.ATTN_EINVAL),
+    (dict(Nk=0), binding.ATTN_EINVAL),
+    (dict(H=3, Hkv=2), binding.ATTN_EINVAL),
+    (dict(scale=0.0), binding.ATTN_EINVAL),
+    (dict(scale=-1.0), binding.ATTN_EINVAL),
+    (dict(scale=float("nan")), binding.ATTN_EINVAL),
+    (dict(scale=float("inf")), binding.ATTN_EINVAL),
+    (dict(causal=2), binding.ATTN_EINVAL),
+    (dict(d=96), binding.ATTN_EUNSUPPORTED),
+    (dict(d=256), binding.ATTN_EUNSUPPORTED),
+    (dict(q=ctypes.c_void_p(0x10008)), binding.ATTN_EINVAL),
+    (dict(lse=ctypes.c_void_p(0x10002)), binding.ATTN_EINVAL),
+])
+def test_attn_fwd_rejects_bad_arguments(lib, kw, status):
+    assert _fwd(lib, **kw) == status
+    assert lib.attn_last_error()
+
+
+def _dec(lib, **kw):
+    a = dict(q=_fake(1), kc=_fake(2), vc=_fake(3), bt=_fake(4), sl=_fake(5), S=4, H=32, Hkv=8,
+             d=128, nb=100, mb=64, bs=16, scale=0.088, o=_fake(6), lse=None, ws=_fake(7),
+             wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.paged_decode(a["q"], a["kc"], a["vc"], a["bt"], a["sl"], a["S"], a["H"], a["Hkv"],
+                            a["d"], a["nb"], a["mb"], a["bs"], a["scale"], a["o"], a["lse"],
+                            a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(bt=None), binding.ATTN_EINVAL),
+    (dict(ws=None), binding.ATTN_EINVAL),
+    (dict(S=0), binding.ATTN_EINVAL),
+    (dict(bs=32), binding.ATTN_EINVAL),
+    (dict(H=30), binding.ATTN_EINVAL),
+    (dict(H=64, Hkv=4), binding.ATTN_EUNSUPPORTED),
+    (dict(d=80), binding.ATTN_EUNSUPPORTED),
+    (dict(wsb=16), binding.ATTN_EINVAL),
+    (dict(scale=0.0), binding.ATTN_EINVAL),
+    (dict(nb=1 << 30), binding.ATTN_EINVAL),
+    (dict(kc=ctypes.c_void_p(0x10004)), binding.ATTN_EINVAL),
+])
+def test_paged_decode_rejects_bad_arguments(lib, kw, status):
+    assert _dec(lib, **kw) == status
+
+
+def test_workspace_size(lib):
+    n = lib.paged_decode_workspace_size(64, 32, 8, 128, 512)
+    # 64 seqs x 32 heads x splits x (d + 2) fp32
+    assert n > 0 and n % (64 * 32 * 130 * 4) == 0
+    assert lib.paged_decode_workspace_size(0, 32, 8, 128, 512) == 0
+    assert lib.paged_decode_workspace_size(64, 30, 8, 128, 512) == 0
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _fwd(lib) in (binding.ATTN_ECUDA, binding.ATTN_EUNSUPPORTED)

@@ -1,0 +1,153 @@
+"""GPU parity of paged_decode (C ABI) against the fp64 oracle.
+
+The oracle works on each sequence's LOGICAL K/V (it never reads the block
+table), so an indexing error on the GPU cannot be cancelled by the same error
+on the reference side.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_fa_attn_fwd_b300 import binding, workloads
+from tests.parity import compare, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu(pb, **kw):
+    o, lse = binding.paged_decode(pb.q.cuda(), pb.k_cache.cuda(), pb.v_cache.cuda(),
+                                  pb.block_table.cuda(), pb.seq_lens.cuda(), **kw)
+    torch.cuda.synchronize()
+    return o.cpu(), lse.cpu()
+
+
+def _ref(pb, scale):
+    ks, vs = [], []
+    for s in range(pb.num_seqs):
+        k, v = pb.logical_kv(s)
+        ks.append(f64(k))
+        vs.append(f64(v))
+    return oracle.paged_decode_ref(f64(pb.q), ks, vs, scale)
+
+
+SMALL = dict(num_seqs=8, H=8, Hkv=2, d=128, block_size=16, min_len=40, max_len=700, group=4,
+             shared_tokens=32, spare_frac=0.1)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("H,Hkv", [(8, 2), (8, 8), (8, 1), (6, 2)])
+def test_small_batch(d, H, Hkv):
+    pb = workloads.paged_decode_inputs(**{**SMALL, "d": d, "H": H, "Hkv": Hkv}, seed=H + Hkv + d)
+    o, lse = _gpu(pb)
+    O, L = _ref(pb, 1 / math.sqrt(d))
+    compare(f64(o), f64(lse), O, L, f"paged d={d} H={H} Hkv={Hkv}")
+
+
+def test_paged_decode_workload_full():
+    cfg = workloads.PAGED_WORKLOADS["paged_decode_s64_h32kv8_d128"]
+    pb = workloads.paged_decode_inputs(**cfg, seed=0)
+    o, lse = _gpu(pb)
+    O, L = _ref(pb, 1 / math.sqrt(cfg["d"]))
+    compare(f64(o), f64(lse), O, L, "paged decode workload")
+
+
+def test_block_table_indexing_exact():
+    # One dominant key per sequence whose V row encodes its logical position:
+    # the bf16 output must equal that row exactly.
+    cfg = dict(workloads.PAGED_WORKLOADS["paged_decode_s64_h32kv8_d128"])
+    pb = workloads.paged_decode_inputs(**cfg, seed=5, index_probe=True)
+    o, _ = _gpu(pb)
+    of = f64(o)
+    for s in range(pb.num_seqs):
+        k, v = pb.logical_kv(s)
+        tgt = int(torch.argmax(k[:, 0, 0].float().abs()))
+        want = f64(v[tgt])  # [Hkv, d]
+        got_t = (of[s, :, 0] - 1) * 64 + (of[s, :, 1] - 1)
+        assert np.all(got_t == tgt), (s, got_t, tgt)
+        G = pb.q.shape[1] // want.shape[0]
+        for h in range(pb.q.shape[1]):
+            assert np.array_equal(of[s, h, :3], want[h // G, :3])
+
+
+@pytest.mark.parametrize("perm_seed", [11, 22, 33])
+def test_physical_permutation_gives_identical_bits(perm_seed):
+    base = workloads.paged_decode_inputs(**SMALL, seed=1)
+    other = workloads.paged_decode_inputs(**SMALL, seed=1, perm_seed=perm_seed)
+    assert not torch.equal(base.block_table, other.block_table)
+    o1, l1 = _gpu(base)
+    o2, l2 = _gpu(other)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_prefix_sharing_gives_identical_bits():
+    shared = workloads.paged_decode_inputs(**SMALL, seed=2, share=True)
+    private = workloads.paged_decode_inputs(**SMALL, seed=2, share=False)
+    o1, l1 = _gpu(shared)
+    o2, l2 = _gpu(private)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_split_count_independence():
+    # A sequence decoded alone (few CTAs -> smaller splits) agrees with the
+    # same sequence inside a large batch within fp32 rounding.
+    pb = workloads.paged_decode_inputs(**{**SMALL, "num_seqs": 16, "max_len": 2000}, seed=3)
+    o_all, l_all = _gpu(pb)
+    s = 5
+    one = workloads.PagedBatch(
+        q=pb.q[s:s + 1].contiguous(), k_cache=pb.k_cache, v_cache=pb.v_cache,
+        block_table=pb.block_table[s:s + 1].contiguous(), seq_lens=pb.seq_lens[s:s + 1].contiguous(),
+        block_size=16, logical_ids=pb.logical_ids[s:s + 1], perm=pb.perm, k_unique=pb.k_unique,
+        v_unique=pb.v_unique, num_unique=pb.num_unique)
+    o1, l1 = _gpu(one)
+    assert np.max(np.abs(f64(o1[0]) - f64(o_all[s]))) <= 1e-2
+    assert np.max(np.abs(f64(l1[0]) - f64(l_all[s]))) <= 1e-4
+
+
+def test_zero_length_and_single_token_sequences():
+    pb = workloads.paged_decode_inputs(**SMALL, seed=4)
+    lens = pb.seq_lens.clone()
+    lens[0] = 0
+    lens[1] = 1
+    lens[2] = 16
+    lens[3] = 17
+    pb2 = workloads.PagedBatch(q=pb.q, k_cache=pb.k_cache, v_cache=pb.v_cache,
+                               block_table=pb.block_table, seq_lens=lens, block_size=16,
+                               logical_ids=pb.logical_ids, perm=pb.perm, k_unique=pb.k_unique,
+                               v_unique=pb.v_unique, num_unique=pb.num_unique)
+    o, lse = _gpu(pb2)
+    assert torch.all(o[0].float() == 0) and torch.all(torch.isneginf(lse[0]))
+    O, L = _ref(pb2, 1 / math.sqrt(128))
+    compare(f64(o[1:]), f64(lse[1:]), O[1:], L[1:], "short sequences")
+
+
+def test_out_of_range_block_id_reports_device_error():
+    pb = workloads.paged_decode_inputs(**SMALL, seed=6)
+    bt = pb.block_table.clone()
+    bt[2, 1] = pb.num_blocks + 5  # read as zeros by the bounded TMA copy
+    o, lse = binding.paged_decode(pb.q.cuda(), pb.k_cache.cuda(), pb.v_cache.cuda(), bt.cuda(),
+                                  pb.seq_lens.cuda())
+    assert binding.device_status() == binding.ATTN_EDEVICE
+    assert binding.device_status() == binding.ATTN_OK  # cleared
+    good = [s for s in range(pb.num_seqs) if s != 2]
+    O, L = _ref(pb, 1 / math.sqrt(128))
+    compare(f64(o.cpu()[good]), f64(lse.cpu()[good]), O[good], L[good], "other sequences")
+
+
+def test_caller_workspace_and_determinism():
+    pb = workloads.paged_decode_inputs(**SMALL, seed=7)
+    S, H, d = pb.q.shape
+    n = binding.paged_decode_workspace_size(S, H, pb.k_cache.shape[1], d, pb.max_blocks_per_seq)
+    ws = torch.full((n,), 255, dtype=torch.uint8, device="cuda")  # garbage contents are fine
+    o1, l1 = binding.paged_decode(pb.q.cuda(), pb.k_cache.cuda(), pb.v_cache.cuda(),
+                                  pb.block_table.cuda(), pb.seq_lens.cuda(), workspace=ws)
+    o2, l2 = binding.paged_decode(pb.q.cuda(), pb.k_cache.cuda(), pb.v_cache.cuda(),
+                                  pb.block_table.cuda(), pb.seq_lens.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    with pytest.raises(binding.AttnError):
+        binding.paged_decode(pb.q.cuda(), pb.k_cache.cuda(), pb.v_cache.cuda(),
+                             pb.block_table.cuda(), pb.seq_lens.cuda(), workspace=ws[:16])
