@@ -69,10 +69,14 @@ def softmax_rows(S: np.ndarray):
 
     Returns (P, m, lse) where m_i = max_j S_ij, P_ij = exp(S_ij - m_i) /
     sum_j exp(S_ij - m_i) and lse_i = m_i + ln sum_j exp(S_ij - m_i).
-    Rows that are entirely -inf give P = 0, m = -inf, lse = -inf.
+    Rows that are entirely -inf, and rows of a zero-width S (no keys), give
+    P = 0, m = -inf, lse = -inf.
     Interview notes "他人面经整理", flashattention answer part 2 (m_i is the row
     maximum, l_i the sum of exp(x - m_i)).
     """
+    if S.shape[1] == 0:  # no keys at all: same as a fully masked row
+        R = S.shape[0]
+        return np.zeros((R, 0)), np.full(R, -np.inf), np.full(R, -np.inf)
     m = S.max(axis=1)
     dead = ~np.isfinite(m)
     m_safe = np.where(dead, 0.0, m)

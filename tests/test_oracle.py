@@ -207,6 +207,14 @@ def test_softmax_rows_all_masked_row():
     assert abs(P[1, 1] - math.e / (1 + math.e)) < 1e-15
 
 
+def test_no_keys_is_a_fully_masked_row():
+    P, m, L = softmax_rows(np.zeros((3, 0)))
+    assert P.shape == (3, 0) and np.all(np.isneginf(m)) and np.all(np.isneginf(L))
+    O, L = oracle.paged_decode_ref(np.ones((1, 2, 4)), [np.zeros((0, 1, 4))],
+                                   [np.zeros((0, 1, 4))], 0.5)
+    assert np.all(O == 0) and np.all(np.isneginf(L))
+
+
 def test_scores_mask_bottom_right():
     q = np.ones((3, 2)); k = np.ones((5, 2))
     S = scores(q, k, 1.0, True, np.arange(3), 3)
