@@ -38,6 +38,8 @@ SIGNATURES = {
     "paged_decode_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "paged_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                           _vp, _vp, _vp, _sz, _vp]),
+    "paged_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
+                                  _vp, _vp, _vp]),
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_device_status": (_i, [_vp]),
 }
@@ -185,6 +187,36 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                           S, H, Hkv, d, num_blocks, max_blocks, block_size, float(scale),
                           o.data_ptr(), lse.data_ptr() if lse is not None else None,
                           workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    _check(st)
+    return o, lse
+
+
+def paged_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         block_table: torch.Tensor, seq_lens: torch.Tensor,
+                         scale: Optional[float] = None, o: Optional[torch.Tensor] = None,
+                         lse: Optional[torch.Tensor] = None,
+                         stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """``paged_decode`` through the entry point that allocates nothing: the
+    library's fixed 32 MiB scratch array replaces the workspace.  Calls that
+    may overlap on the GPU race on that array; keep them on one stream."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    S, H, d = q.shape
+    num_blocks, Hkv, block_size, _ = k_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((S, H), dtype=torch.float32, device=q.device)
+    st = lib.paged_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                  block_table.data_ptr(), seq_lens.data_ptr(), S, H, Hkv, d,
+                                  num_blocks, block_table.shape[1], block_size, float(scale),
+                                  o.data_ptr(), lse.data_ptr(), _stream_handle(stream))
     _check(st)
     return o, lse
 

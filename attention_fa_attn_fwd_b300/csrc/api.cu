@@ -103,6 +103,13 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64
   return true;
 }
 
+void set_last_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+}
+
 }  // namespace attn
 
 extern "C" {

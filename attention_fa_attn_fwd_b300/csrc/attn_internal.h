@@ -34,4 +34,7 @@ cudaError_t decode_launch(const void* q, const void* k_cache, const void* v_cach
                           cudaStream_t stream, const char** err);
 int decode_take_device_error();
 
+// Sets the calling thread's attn_last_error() message (printf-style).
+void set_last_error(const char* fmt, ...);
+
 }  // namespace attn

@@ -125,6 +125,30 @@ ATTN_API attn_status paged_decode(const void* q, const void* k_cache, const void
                          float scale, void* o, float* lse, void* workspace,
                          size_t workspace_bytes, attn_stream_t stream);
 
+/*
+ * paged_decode_noalloc -- paged_decode for callers that cannot allocate
+ * device memory (the source pages have no counterpart of this call).
+ *
+ * Some callers may not call cudaMalloc: a plugin whose host framework passes
+ * it only input and output buffers, or a serving process that reserves all
+ * device memory for its KV pool at start-up.  This call takes the same
+ * arguments as paged_decode minus the workspace, and uses a 32 MiB scratch
+ * array compiled into the library instead; it allocates nothing.
+ *   - Sizes whose paged_decode_workspace_size() exceeds 32 MiB are rejected
+ *     with ATTN_EINVAL (use paged_decode with a caller workspace then).
+ *   - The array exists on every GPU that loads the library, until exit.
+ *   - All calls share it: calls whose kernels can overlap on the GPU (two
+ *     streams, or two host threads on one device) race and give wrong
+ *     results.  Serialise them on one stream.
+ *   - The first call on each device looks the array's address up (once, with
+ *     that device current); make that first call before any stream capture.
+ */
+ATTN_API attn_status paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* block_table, const int32_t* seq_lens,
+                                          int num_seqs, int H, int Hkv, int d, int num_blocks,
+                                          int max_blocks_per_seq, int block_size, float scale,
+                                          void* o, float* lse, attn_stream_t stream);
+
 /* Message for the last non-OK status returned on the calling thread. */
 ATTN_API const char* attn_last_error(void);
 

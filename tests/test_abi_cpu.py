@@ -28,7 +28,8 @@ def lib():
 
 def test_header_declares_expected_api():
     assert declared_functions() == sorted(["attn_fwd", "paged_decode", "paged_decode_workspace_size",
-                                           "attn_last_error", "attn_device_status"])
+                                           "paged_decode_noalloc", "attn_last_error",
+                                           "attn_device_status"])
 
 
 def test_every_declared_symbol_is_exported(lib):
