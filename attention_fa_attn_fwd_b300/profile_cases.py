@@ -1,0 +1,69 @@
+"""Run one hot-path workload a fixed number of times (for Nsight Compute).
+
+    python -m attention_fa_attn_fwd_b300.profile_cases --case prefill --iters 3
+    python -m attention_fa_attn_fwd_b300.profile_cases --case decode --iters 3
+    python -m attention_fa_attn_fwd_b300.profile_cases --case step --iters 3
+
+``prefill``: attn_fwd on the long-context causal GQA workload (B1 H32 Hkv8
+N16384 d128; 335 MB on the device, larger than L2).  ``decode``: paged_decode
+on the 64-sequence workload (2.3 GB pool).  ``step``: both, as one bench step.
+A 256 MiB L2 flush (a memset, not one of this library's kernels) precedes
+every kernel, as in bench.py.  Prints the CUDA-event time of each launch.
+"""
+
+from __future__ import annotations
+
+import argparse
+import math
+
+import torch
+
+from . import binding, workloads
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", choices=["prefill", "decode", "step"], default="step")
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--prefill", default="gqa_b1h32kv8_n16384_d128_causal")
+    ap.add_argument("--decode-seqs", type=int, default=64,
+                    help="sequences of the decode workload (fewer: smaller pool for long captures)")
+    args = ap.parse_args(argv)
+    binding.load_library()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    runs = []
+    if args.case in ("prefill", "step"):
+        cfg = dict(workloads.PREFILL_WORKLOADS.get(args.prefill) or workloads.sweep_workloads()[args.prefill])
+        q, k, v = (t.to(dev) for t in workloads.prefill_inputs(**cfg))
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        runs.append(("attn_fwd", lambda: binding.attn_fwd(q, k, v, causal=cfg["causal"], o=o, lse=lse)))
+    if args.case in ("decode", "step"):
+        dcfg = dict(workloads.PAGED_WORKLOADS["paged_decode_s64_h32kv8_d128"])
+        dcfg["num_seqs"] = args.decode_seqs
+        pb = workloads.paged_decode_inputs(**dcfg)
+        dq, kc, vc = pb.q.to(dev), pb.k_cache.to(dev), pb.v_cache.to(dev)
+        bt, sl = pb.block_table.to(dev), pb.seq_lens.to(dev)
+        do = torch.empty_like(dq)
+        dl = torch.empty(dq.shape[:2], dtype=torch.float32, device=dev)
+        n = binding.paged_decode_workspace_size(dq.shape[0], dq.shape[1], kc.shape[1], dq.shape[2],
+                                                bt.shape[1])
+        ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        runs.append(("paged_decode", lambda: binding.paged_decode(dq, kc, vc, bt, sl, o=do, lse=dl,
+                                                                  workspace=ws)))
+    for it in range(args.iters):
+        for name, fn in runs:
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            print(f"{name} iter {it}: {a.elapsed_time(b):.3f} ms", flush=True)
+    assert binding.device_status() == 0
+
+
+if __name__ == "__main__":
+    main()
