@@ -7,22 +7,31 @@
 // notes "他人面经整理", flashattention answer part 2: kernel fusion, tiling,
 // online softmax with running max m and running sum l).
 //
-// One CTA owns one 128-row Q tile of one (batch, head) and streams all of the
-// K/V tiles it may attend (causal: up to the diagonal).  Warp roles:
-//   warp 0      TMA producer: Q once, then K_j / V_j into a ring of stages
+// One CTA owns two 128-row Q tiles (Q0, Q1) of one (batch, head) and streams
+// every K/V tile either may attend (causal: up to the diagonal); each K/V tile
+// is read from shared memory by both Q tiles.  Warp roles (12 warps, three
+// warpgroups; warpgroup 0 gives registers to the other two via setmaxnreg):
+//   warp 0      TMA producer: Q0, Q1 once, then K_j / V_j into rings of stages
 //               (the double-buffered prefetch of the FSA page, section 3.2).
-//   warp 1      tcgen05 MMA issuer (one thread): S_j = Q K_j^T into TMEM,
-//               O += P_j V_j with P_j read from TMEM.
-//   warps 2..5  softmax: thread r owns TMEM lane / Q row r.  Online softmax in
-//               base 2 with scale*log2(e) folded into one FFMA; the running
-//               max is only moved when it grows by more than 8 (log2 units),
-//               and O in TMEM is rescaled only then; P is written back to
-//               TMEM as bf16.  At the end: O / l (deferred normalisation),
-//               bf16 O through smem and a TMA store, lse = (m + log2 l) ln 2.
+//   warp 1      tcgen05 MMA issuer: S_i = Q_i K_j^T into TMEM, O_i += P_i V_j
+//               with P_i read from TMEM.  Issue order per KV tile j:
+//               PV(0,j) QK(0,j+1) PV(1,j) QK(1,j+1), so while one softmax
+//               warpgroup works on tile i the tensor pipe runs the other's.
+//   warps 2..3  idle.
+//   warps 4..7  softmax warpgroup of Q0, warps 8..11 of Q1: thread r owns TMEM
+//               lane / Q row r.  Online softmax in base 2 with scale*log2(e)
+//               folded into one FFMA; the running max only moves when it
+//               grows by more than 8 (log2 units) and only then is O_i
+//               rescaled in TMEM; P_i is written back to TMEM as bf16 over
+//               the S_i columns it came from.  At the end: O_i / l (deferred
+//               normalisation), bf16 O through smem and a TMA store,
+//               lse = (m + log2 l) ln 2.
 //
-// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P0 [384,448) P1 [448,512).
-// The mbarrier protocol and why each wait is sufficient is described next to
-// each role below.  Every wait is bounded (ptx.cuh).
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d);
+// P_i occupies the first 64 columns of S_i.  tcgen05.mma operations of one
+// issuing thread execute in order, so QK(i,j+1) overwriting P_i happens after
+// PV(i,j) read it, and "S_i(j+1) complete" implies "PV(i,j) complete".
+// Every wait is bounded (ptx.cuh).
 
 #include <cmath>
 #include <cstdio>
@@ -40,46 +49,56 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 template <int D>
 struct Cfg {
-  static constexpr int kSlabs = D / 64;          // 64-element (128-byte) column slabs
-  static constexpr int kSlabBytes = 128 * 128;   // 128 rows x 128 B
-  static constexpr int kTileBytes = kSlabs * kSlabBytes;
-  static constexpr int kStages = (D == 128) ? 3 : 4;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kSlabs = D / 64;         // 64-element (128-byte) column slabs
+  static constexpr int kSlabBytes = 128 * 128;  // 128 rows x 128 B
+  static constexpr int kTileBytes = kSlabs * kSlabBytes;  // one 128-row Q, K or V tile
+  static constexpr int kKStages = (D == 128) ? 3 : 4;
+  static constexpr int kVStages = (D == 128) ? 2 : 4;
+  static constexpr int kOffQ = 0;  // Q0, Q1 (reused as O0, O1 staging)
+  static constexpr int kOffK = 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   // barrier indices
-  static constexpr int kBarQ = 0;
-  static constexpr int kBarKF = 1;
-  static constexpr int kBarKE = kBarKF + kStages;
-  static constexpr int kBarVF = kBarKE + kStages;
-  static constexpr int kBarVE = kBarVF + kStages;
-  static constexpr int kBarSF = kBarVE + kStages;  // 2
-  static constexpr int kBarPF = kBarSF + 2;        // 2: P_j written (softmax -> MMA)
-  static constexpr int kBarPE = kBarPF + 2;        // 2: PV_j done (MMA -> softmax)
-  static constexpr int kBarDrain = kBarPE + 2;
+  static constexpr int kBarQF = 0;                    // 2: Q_i loaded
+  static constexpr int kBarKF = kBarQF + 2;           // K stage full
+  static constexpr int kBarKE = kBarKF + kKStages;    // K stage free
+  static constexpr int kBarVF = kBarKE + kKStages;    // V stage full
+  static constexpr int kBarVE = kBarVF + kVStages;    // V stage free
+  static constexpr int kBarSF = kBarVE + kVStages;    // 2: S_i ready in TMEM
+  static constexpr int kBarPF = kBarSF + 2;           // 2: P_i written (and O_i rescaled)
+  static constexpr int kBarOF = kBarPF + 2;           // 2: last PV of tile i done
+  static constexpr int kBarDrain = kBarOF + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-B alignment
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;
-  static constexpr uint32_t kColO = 256;
-  static constexpr uint32_t kColP = 384;
-  static constexpr int kThreads = 192;
+  static constexpr uint32_t kColS = 0;    // S_i at i * 128
+  static constexpr uint32_t kColO = 256;  // O_i at 256 + i * D
+  static constexpr int kThreads = 384;
+  // Registers per thread: 168 at launch (64K / 384); warpgroup 0 drops to
+  // 80, the two softmax warpgroups rise to 208 (128*80 + 256*208 <= 384*168).
+  static constexpr int kRegsLow = 80;
+  static constexpr int kRegsHigh = 208;
 };
 
 struct Args {
   float* lse;
   int B, H, Hkv, Nq, Nk;
-  int n_qtiles;
+  int n_pairs;   // ceil(Nq / 256)
   float c_log2;  // scale * log2(e)
   int causal;
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(384, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
@@ -97,33 +116,31 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Heavy (late, causal) Q tiles first; heads of one KV group adjacent.
+  // Heavy (late, causal) tile pairs first; heads of one KV group adjacent.
   const int BH = a.B * a.H;
   const int bh = blockIdx.x % BH;
-  const int qt = a.n_qtiles - 1 - blockIdx.x / BH;
-  const int q0 = qt * 128;
+  const int q0 = (a.n_pairs - 1 - int(blockIdx.x / BH)) * 256;
   const int b = bh / a.H;
   const int h = bh % a.H;
   const int zkv = b * a.Hkv + h / (a.H / a.Hkv);
-  int kv_end = a.Nk;
-  if (a.causal) kv_end = min(a.Nk, q0 + 128 + (a.Nk - a.Nq));
   const bool dead = timed_out_before(err);
-  const int n_tiles = (kv_end > 0 && !dead) ? (kv_end + 127) / 128 : 0;
+  // KV tiles each Q tile attends (0 for a tile past Nq or fully masked).
+  int n_t[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r0 = q0 + i * 128;
+    int kv_end = a.Nk;
+    if (a.causal) kv_end = min(a.Nk, r0 + 128 + (a.Nk - a.Nq));
+    n_t[i] = (r0 < a.Nq && kv_end > 0 && !dead) ? (kv_end + 127) / 128 : 0;
+  }
+  const int n_kv = max(n_t[0], n_t[1]);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(C::kBarQ), 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(C::kBarKF + s), 1);
-      mbar_init(bar(C::kBarKE + s), 1);
-      mbar_init(bar(C::kBarVF + s), 1);
-      mbar_init(bar(C::kBarVE + s), 1);
+    for (int i = 0; i < C::kNumBars; ++i) {
+      uint32_t count = 1;
+      if (i == C::kBarPF || i == C::kBarPF + 1) count = 128;
+      mbar_init(bar(i), count);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(C::kBarSF + i), 1);
-      mbar_init(bar(C::kBarPF + i), 128);
-      mbar_init(bar(C::kBarPE + i), 1);
-    }
-    mbar_init(bar(C::kBarDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -142,124 +159,160 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ---------------------------------------------------------- producer
-    // K_j goes to stage j % S once QK_{j-S} has finished reading it (K-empty,
-    // committed by the MMA warp); V_j likewise once PV_{j-S} has finished.
-    if (lane == 0 && n_tiles > 0) {
-      int k_issued = 0, v_issued = 0;
-      bool ok = true;
-      mbar_arrive_expect_tx(bar(C::kBarQ), C::kTileBytes);
-      for (int s = 0; s < C::kSlabs; ++s)
-        tma_load_3d(sbase + C::kOffQ + s * C::kSlabBytes, &tm_q, bar(C::kBarQ), s * 64, q0, bh);
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % C::kStages;
-        const uint32_t ph = (j / C::kStages) & 1;
-        ok = mbar_wait(bar(C::kBarKE + st), ph ^ 1, abort_flag, err, kErrTimeoutProducer);
-        if (!ok) break;
-        mbar_arrive_expect_tx(bar(C::kBarKF + st), C::kTileBytes);
-        for (int s = 0; s < C::kSlabs; ++s)
-          tma_load_3d(sbase + C::kOffK + st * C::kTileBytes + s * C::kSlabBytes, &tm_k,
-                      bar(C::kBarKF + st), s * 64, j * 128, zkv);
-        k_issued = j + 1;
-        ok = mbar_wait(bar(C::kBarVE + st), ph ^ 1, abort_flag, err, kErrTimeoutProducer);
-        if (!ok) break;
-        mbar_arrive_expect_tx(bar(C::kBarVF + st), C::kTileBytes);
-        for (int s = 0; s < C::kSlabs; ++s)
-          tma_load_3d(sbase + C::kOffV + st * C::kTileBytes + s * C::kSlabBytes, &tm_v,
-                      bar(C::kBarVF + st), s * 64, j * 128, zkv);
-        v_issued = j + 1;
-      }
-      if (!ok) {
-        // Abort path: let every copy already in flight land before exit.
-        const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
-        mbar_wait_drain(bar(C::kBarQ), 0, deadline);
-        for (int j = max(0, k_issued - C::kStages); j < k_issued; ++j)
-          mbar_wait_drain(bar(C::kBarKF + j % C::kStages), (j / C::kStages) & 1, deadline);
-        for (int j = max(0, v_issued - C::kStages); j < v_issued; ++j)
-          mbar_wait_drain(bar(C::kBarVF + j % C::kStages), (j / C::kStages) & 1, deadline);
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    // Order: QK_0, then for each j: QK_{j+1}, PV_j.  QK_{j+1} writes S buffer
-    // (j+1)&1, last read by softmax_{j-1}, which finished before PV_{j-1} was
-    // issued (P-full wait).  PV_j reads P buffer j&1 and accumulates into O.
-    if (lane == 0 && n_tiles > 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 1);
-      bool ok = mbar_wait(bar(C::kBarQ), 0, abort_flag, err, kErrTimeoutMma);
-      auto issue_qk = [&](int j) -> bool {
-        const int st = j % C::kStages;
-        if (!mbar_wait(bar(C::kBarKF + st), (j / C::kStages) & 1, abort_flag, err, kErrTimeoutMma))
-          return false;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + C::kColS + (j & 1) * 128;
+  if (warp < 4) {
+    setmaxnreg_dec<C::kRegsLow>();
+    if (warp == 0) {
+      // -------------------------------------------------------- producer
+      // The whole warp runs this loop; one elected lane issues each copy.
+      // K_j goes to K stage j % KS once its previous occupant K_{j-KS} has
+      // been consumed by its last QK (K-empty, committed by the MMA warp);
+      // V_j likewise after the last PV of V_{j-VS}.
+      if (n_kv > 0) {
+        int k_issued = 0, v_issued = 0;
+        bool ok = true;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kSlabBytes + (kk & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(sbase + C::kOffQ + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(sbase + C::kOffK + st * C::kTileBytes + off, 16, 1024);
-          mma_bf16_ss(d_tmem, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+        for (int i = 0; i < 2; ++i) {
+          if (n_t[i] == 0) continue;
+          mbar_arrive_expect_tx_elect(bar(C::kBarQF + i), C::kTileBytes);
+          for (int s = 0; s < C::kSlabs; ++s)
+            tma_load_3d_elect(sbase + C::kOffQ + i * C::kTileBytes + s * C::kSlabBytes, &tm_q,
+                              bar(C::kBarQF + i), s * 64, q0 + i * 128, bh);
         }
-        mma_commit(bar(C::kBarSF + (j & 1)));
-        mma_commit(bar(C::kBarKE + st));
-        return true;
-      };
-      auto issue_pv = [&](int j) -> bool {
-        const int st = j % C::kStages;
-        if (!mbar_wait(bar(C::kBarPF + (j & 1)), (j >> 1) & 1, abort_flag, err, kErrTimeoutMma))
-          return false;
-        if (!mbar_wait(bar(C::kBarVF + st), (j / C::kStages) & 1, abort_flag, err, kErrTimeoutMma))
-          return false;
-        tc_fence_after();
-        const uint32_t a_tmem = tmem + C::kColP + (j & 1) * 64;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // V tile is [128 keys][D] in 64-column slabs: B operand MN-major,
-          // 16 keys per MMA = 2 swizzle atoms of 8 rows (SBO 1024), next
-          // 64 output columns one slab further (LBO = slab size).
-          const uint64_t bd = smem_desc_sw128(sbase + C::kOffV + st * C::kTileBytes + kk * 2048,
-                                              C::kSlabBytes, 1024);
-          mma_bf16_ts(tmem + C::kColO, a_tmem + kk * 8, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int j = 0; j < n_kv; ++j) {
+          const int ks = j % C::kKStages, vs = j % C::kVStages;
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(bar(C::kBarKE + ks), ((j / C::kKStages) & 1) ^ 1, abort_flag,
+                                    err, kErrTimeoutProducer));
+          if (!ok) break;
+          mbar_arrive_expect_tx_elect(bar(C::kBarKF + ks), C::kTileBytes);
+          for (int s = 0; s < C::kSlabs; ++s)
+            tma_load_3d_elect(sbase + C::kOffK + ks * C::kTileBytes + s * C::kSlabBytes, &tm_k,
+                              bar(C::kBarKF + ks), s * 64, j * 128, zkv);
+          k_issued = j + 1;
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(bar(C::kBarVE + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag,
+                                    err, kErrTimeoutProducer));
+          if (!ok) break;
+          mbar_arrive_expect_tx_elect(bar(C::kBarVF + vs), C::kTileBytes);
+          for (int s = 0; s < C::kSlabs; ++s)
+            tma_load_3d_elect(sbase + C::kOffV + vs * C::kTileBytes + s * C::kSlabBytes, &tm_v,
+                              bar(C::kBarVF + vs), s * 64, j * 128, zkv);
+          v_issued = j + 1;
         }
-        mma_commit(bar(C::kBarVE + st));
-        mma_commit(bar(C::kBarPE + (j & 1)));
-        return true;
-      };
-      if (ok) ok = issue_qk(0);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles) ok = issue_qk(j + 1);
-        if (ok) ok = issue_pv(j);
+        if (!ok) {
+          // Abort path: let every copy already in flight land before exit.
+          const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
+          for (int i = 0; i < 2; ++i)
+            if (n_t[i] > 0) mbar_wait_drain(bar(C::kBarQF + i), 0, deadline);
+          for (int j = max(0, k_issued - C::kKStages); j < k_issued; ++j)
+            mbar_wait_drain(bar(C::kBarKF + j % C::kKStages), (j / C::kKStages) & 1, deadline);
+          for (int j = max(0, v_issued - C::kVStages); j < v_issued; ++j)
+            mbar_wait_drain(bar(C::kBarVF + j % C::kVStages), (j / C::kVStages) & 1, deadline);
+        }
       }
-      if (!ok) {
-        // Abort path: no MMA may be in flight when TMEM is released.
-        mma_commit(bar(C::kBarDrain));
-        mbar_wait_drain(bar(C::kBarDrain), 0, globaltimer_ns() + kWaitTimeoutNs);
+    } else if (warp == 1) {
+      // -------------------------------------------------------- MMA issuer
+      // The whole warp runs this loop; one elected lane issues each MMA.
+      if (n_kv > 0) {
+        constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0);
+        constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 1);
+        // Base descriptors; per-step offsets go into the 16-byte address field.
+        const uint64_t q_desc = smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
+        const uint64_t k_desc = smem_desc_sw128(sbase + C::kOffK, 16, 1024);
+        const uint64_t v_desc = smem_desc_sw128(sbase + C::kOffV, C::kSlabBytes, 1024);
+        bool ok = true;
+        // S_i = Q_i K_j^T.  The last Q tile using K_j frees its stage.
+        auto issue_qk = [&](int i, int j) -> bool {
+          const int ks = j % C::kKStages;
+          if (j == 0 && !__all_sync(0xffffffffu, mbar_wait(bar(C::kBarQF + i), 0, abort_flag, err,
+                                                           kErrTimeoutMma)))
+            return false;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarKF + ks), (j / C::kKStages) & 1,
+                                                 abort_flag, err, kErrTimeoutMma)))
+            return false;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + C::kColS + i * 128;
+          const uint64_t qo = uint64_t((i * C::kTileBytes) >> 4);
+          const uint64_t ko = uint64_t((ks * C::kTileBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
+            mma_bf16_ss(d_tmem, q_desc + qo + off, k_desc + ko + off, kIdescQK, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(C::kBarSF + i));
+          if (i == 1 || j >= n_t[1]) mma_commit(bar(C::kBarKE + ks));
+          return true;
+        };
+        // O_i += P_i V_j, P_i read from the first 64 TMEM columns of S_i.
+        auto issue_pv = [&](int i, int j) -> bool {
+          const int vs = j % C::kVStages;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF + i), j & 1, abort_flag, err,
+                                                 kErrTimeoutMma)))
+            return false;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarVF + vs), (j / C::kVStages) & 1,
+                                                 abort_flag, err, kErrTimeoutMma)))
+            return false;
+          tc_fence_after();
+          const uint32_t a_tmem = tmem + C::kColS + i * 128;
+          const uint64_t vo = uint64_t((vs * C::kTileBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // V tile is [128 keys][D] in 64-column slabs: B operand MN-major,
+            // 16 keys per MMA = 2 swizzle atoms of 8 rows (SBO 1024), next
+            // 64 output columns one slab further (LBO = slab size).
+            mma_bf16_ts(tmem + C::kColO + i * D, a_tmem + kk * 8,
+                        v_desc + vo + uint64_t((kk * 2048) >> 4), kIdescPV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (i == 1 || j >= n_t[1]) mma_commit(bar(C::kBarVE + vs));
+          if (j == n_t[i] - 1) mma_commit(bar(C::kBarOF + i));
+          return true;
+        };
+        if (n_t[0] > 0) ok = issue_qk(0, 0);
+        if (ok && n_t[1] > 0) ok = issue_qk(1, 0);
+        for (int j = 0; ok && j < n_kv; ++j) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            if (ok && j < n_t[i]) {
+              ok = issue_pv(i, j);
+              if (ok && j + 1 < n_t[i]) ok = issue_qk(i, j + 1);
+            }
+          }
+        }
+        if (!ok) {
+          // Abort path: no MMA may be in flight when TMEM is released.
+          mma_commit(bar(C::kBarDrain));
+          mbar_wait_drain(bar(C::kBarDrain), 0, globaltimer_ns() + kWaitTimeoutNs);
+        }
       }
     }
   } else {
+    setmaxnreg_inc<C::kRegsHigh>();
     // ---------------------------------------------------------- softmax
-    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int wg = (warp >> 2) - 1;  // Q tile of this warpgroup
+    const int quarter = warp & 3;    // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
-    const int q_row = q0 + row;
+    const uint32_t col_s = C::kColS + wg * 128;
+    const uint32_t col_o = C::kColO + wg * D;
+    const int n = n_t[wg];
+    const int q_row = q0 + wg * 128 + row;
     // Last key this row may attend (bottom-right causal alignment).
     const int row_last = a.causal ? min(a.Nk - 1, q_row + (a.Nk - a.Nq)) : (a.Nk - 1);
     const float c = a.c_log2;
     float m = -INFINITY;  // reference maximum, log2 units of the scaled score
     float l = 0.f;        // running sum of 2^(s*c - m)
     bool ok = !dead;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int buf = j & 1;
-      ok = mbar_wait(bar(C::kBarSF + buf), (j >> 1) & 1, abort_flag, err, kErrTimeoutSoftmax);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+    for (int j = 0; j < n; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarSF + wg), j & 1, abort_flag, err,
+                                             kErrTimeoutSoftmax));
+      if (!ok) break;
       tc_fence_after();
       uint32_t s[128];
-      tmem_ld32(lane_base + C::kColS + buf * 128 + 0, s + 0);
-      tmem_ld32(lane_base + C::kColS + buf * 128 + 32, s + 32);
-      tmem_ld32(lane_base + C::kColS + buf * 128 + 64, s + 64);
-      tmem_ld32(lane_base + C::kColS + buf * 128 + 96, s + 96);
+      tmem_ld32(lane_base + col_s + 0, s + 0);
+      tmem_ld32(lane_base + col_s + 32, s + 32);
+      tmem_ld32(lane_base + col_s + 64, s + 64);
+      tmem_ld32(lane_base + col_s + 96, s + 96);
       tmem_ld_wait();
       reg_fence<128>(s);
 
@@ -274,9 +327,14 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i]);
 #pragma unroll
-      for (int cc = 8; cc < 128; ++cc) mx[cc & 7] = fmaxf(mx[cc & 7], __uint_as_float(s[cc]));
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
+      for (int cc = 8; cc < 120; cc += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          mx[i] = max3f(mx[i], __uint_as_float(s[cc + i]), __uint_as_float(s[cc + 8 + i]));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(s[120 + i]));
+      const float mt =
+          max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c;
       // Move the reference only when the max grew by more than the threshold
       // (or on the first finite max).  alpha rescales l and O.
       const bool move = mt > m + kRescaleThreshold;
@@ -287,66 +345,63 @@ __global__ void __launch_bounds__(192, 1)
         l *= alpha;
       }
       if (j > 0 && __any_sync(0xffffffffu, move)) {
-        // O must not be in flight: wait for PV_{j-1}.
-        ok = mbar_wait(bar(C::kBarPE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, err,
-                       kErrTimeoutSoftmax);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
+        // S_i(j) complete implies PV(i, j-1) complete: O_i is not in flight.
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
-          tmem_ld32(lane_base + C::kColO + c0, o);
+          tmem_ld32(lane_base + col_o + c0, o);
           tmem_ld_wait();
           reg_fence<32>(o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(lane_base + C::kColO + c0, o);
+          tmem_st32(lane_base + col_o + c0, o);
         }
-        tmem_st_wait();
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float rs[8];
+      const float2 c2 = make_float2(c, c);
+      const float2 nm2 = make_float2(neg_m, neg_m);
+      float2 acc[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) rs[i] = 0.f;
-      uint32_t pk[64];
+      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int cc = 0; cc < 128; cc += 2) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(s[cc]), c, neg_m));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(s[cc + 1]), c, neg_m));
-        rs[(cc >> 1) & 7] += p0 + p1;
-        pk[cc >> 1] = pack_bf16x2(p0, p1);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int cc = half * 64 + 2 * e;
+          float2 x = __ffma2_rn(make_float2(__uint_as_float(s[cc]), __uint_as_float(s[cc + 1])),
+                                c2, nm2);
+          x.x = ex2_approx(x.x);
+          x.y = ex2_approx(x.y);
+          acc[e & 3] = __fadd2_rn(acc[e & 3], x);
+          pk[e] = pack_bf16x2(x.x, x.y);
+        }
+        // P over the S columns (S is already in registers).
+        tmem_st32(lane_base + col_s + half * 32, pk);
       }
-      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-      if (j >= 2) {
-        // P buffer `buf` was last read by PV_{j-2}.
-        ok = mbar_wait(bar(C::kBarPE + buf), ((j - 2) >> 1) & 1, abort_flag, err,
-                       kErrTimeoutSoftmax);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-      }
-      __syncwarp();
-      tmem_st32(lane_base + C::kColP + buf * 64, pk);
-      tmem_st32(lane_base + C::kColP + buf * 64 + 32, pk + 32);
+      const float2 t01 = __fadd2_rn(acc[0], acc[1]);
+      const float2 t23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 t = __fadd2_rn(t01, t23);
+      l += t.x + t.y;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::kBarPF + buf));
+      mbar_arrive(bar(C::kBarPF + wg));
     }
 
     // ---------------------------------------------------------- epilogue
-    if (ok && n_tiles > 0) {
-      ok = mbar_wait(bar(C::kBarPE + ((n_tiles - 1) & 1)), ((n_tiles - 1) >> 1) & 1, abort_flag,
-                     err, kErrTimeoutEpilogue);
-      ok = __all_sync(0xffffffffu, ok);
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::kBarOF + wg), 0, abort_flag, err, kErrTimeoutEpilogue));
       tc_fence_after();
     }
+    uint8_t* stage = smem + C::kOffQ + wg * C::kTileBytes;  // Q_i is no longer read
     if (ok) {
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      uint8_t* stage = smem + C::kOffQ;  // Q is no longer read: every MMA is done
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
-        if (n_tiles > 0) {
-          tmem_ld32(lane_base + C::kColO + c0, o);
+        if (n > 0) {
+          tmem_ld32(lane_base + col_o + c0, o);
           tmem_ld_wait();
           reg_fence<32>(o);
         } else {
@@ -368,11 +423,12 @@ __global__ void __launch_bounds__(192, 1)
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(1 + wg, 128);
     if (!*abort_flag && ok) {
-      if (warp == 2 && lane == 0) {
+      if (quarter == 0 && lane == 0) {
         for (int s = 0; s < C::kSlabs; ++s)
-          tma_store_3d(&tm_o, sbase + C::kOffQ + s * C::kSlabBytes, s * 64, q0, bh);
+          tma_store_3d(&tm_o, sbase + C::kOffQ + wg * C::kTileBytes + s * C::kSlabBytes, s * 64,
+                       q0 + wg * 128, bh);
         bulk_commit_group();
         bulk_wait_group_read0();
       }
@@ -422,10 +478,10 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
   a.Hkv = Hkv;
   a.Nq = Nq;
   a.Nk = Nk;
-  a.n_qtiles = (Nq + 127) / 128;
+  a.n_pairs = (Nq + 255) / 256;
   a.c_log2 = scale * kLog2e;
   a.causal = causal;
-  const unsigned grid = unsigned(a.n_qtiles) * unsigned(B) * unsigned(H);
+  const unsigned grid = unsigned(a.n_pairs) * unsigned(B) * unsigned(H);
   prefill_fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
