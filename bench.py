@@ -330,13 +330,15 @@ def run_ours(args, ws, rank, local):
     d_mean = max_over_ranks(statistics.mean(d_ms), ws)
     assert binding.device_status(stream) == 0
 
-    flops = prefill_flops(cfg)
+    # Whole-job throughput: every rank ran the same step (independent replicas),
+    # timed by the slowest rank.
+    flops = prefill_flops(cfg) * ws
     tflops = flops / (p_mean * 1e-3) / 1e12
     per_tok = kc.shape[1] * kc.shape[3] * 2 * 2
     uniq_bytes = pb.unique_valid_tokens() * per_tok
     logical_bytes = pb.logical_tokens() * per_tok
     small_bytes = (dq.numel() * 2 * 2 + bt.numel() * 4 + sl.numel() * 4 + dlse.numel() * 4)
-    dec_gbs = (uniq_bytes + small_bytes) / (d_mean * 1e-3) / 1e9
+    dec_gbs = ws * (uniq_bytes + small_bytes) / (d_mean * 1e-3) / 1e9
 
     # ---- end to end through the public API with pinned host buffers
     qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
@@ -377,7 +379,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     ep = max_over_ranks(statistics.mean(e_evs[i][0].elapsed_time(e_evs[i][1]) for i in range(Ke)), ws)
     ed = max_over_ranks(statistics.mean(e_evs[i][1].elapsed_time(e_evs[i][2]) for i in range(Ke)), ws)
-    e2e_tflops = flops / (ep * 1e-3) / 1e12
+    e2e_tflops = flops / (ep * 1e-3) / 1e12  # flops already counts every rank
 
     if rank != 0:
         return
@@ -386,6 +388,8 @@ def run_ours(args, ws, rank, local):
     cpu_tf, cpu_desc, _, _ = oracle_prefill_sample(q_h, k_h, v_h, cfg, args.cpu_budget)
     cpu_dec, cpu_ddesc, _ = oracle_decode_sample(pb, max(1.0, args.cpu_budget / 4))
     peak_tf = peaks["bf16_tflops"]
+    k_tflops = tflops / ws  # one replica's kernel against one GPU's peak
+    k_gbs = dec_gbs / ws
     line = {
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": p_mean + d_mean, "higher_is_better": True,
@@ -393,22 +397,22 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": f"{PREFILL} + {DECODE}", "prefill": cfg, "decode": dcfg,
                    "l2": "256 MiB L2 flush before every kernel (outside the events)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
-        "prefill": {"ms": p_mean, "tflops": tflops, "frac_burst": tflops / peak_tf,
-                    "frac_sustained": tflops / peaks["bf16_tflops_sustained"]},
+        "prefill": {"ms": p_mean, "tflops": tflops, "frac_burst": k_tflops / peak_tf,
+                    "frac_sustained": k_tflops / peaks["bf16_tflops_sustained"]},
         "decode": {"ms": d_mean, "value": dec_gbs, "unit": "GB/s",
                    "unique_kv_bytes": uniq_bytes, "logical_kv_bytes": logical_bytes,
-                   "logical_gbs": (logical_bytes + small_bytes) / (d_mean * 1e-3) / 1e9,
-                   "frac_hbm_measured": dec_gbs / peaks["hbm_gbs"], "frac_hbm_8tbs": dec_gbs / 8000.0},
-        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": tflops / peak_tf, "traffic": traffic,
+                   "logical_gbs": ws * (logical_bytes + small_bytes) / (d_mean * 1e-3) / 1e9,
+                   "frac_hbm_measured": k_gbs / peaks["hbm_gbs"], "frac_hbm_8tbs": k_gbs / 8000.0},
+        "roofline": {"bound": "tensor", "achieved": k_tflops, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": k_tflops / peak_tf, "traffic": traffic,
                      "kernel": "prefill_fwd_kernel<128>", "peak_kind": f"bf16 burst ({peaks['source']})"},
-        "roofline_decode": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
-                            "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
+        "roofline_decode": {"bound": "hbm", "achieved": k_gbs, "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s", "frac": k_gbs / peaks["hbm_gbs"],
                             "traffic": committed_traffic("decode_split_kernel", ["decode_sm103.cu", "ptx.cuh"]),
                             "kernel": "decode_split_kernel<128> + decode_merge_kernel<128>"},
         "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "prefill_ms": ep, "decode_ms": ed,
-                "decode_gbs": (uniq_bytes + small_bytes) / (ed * 1e-3) / 1e9},
+                "decode_gbs": ws * (uniq_bytes + small_bytes) / (ed * 1e-3) / 1e9},
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": blas_threads(),
