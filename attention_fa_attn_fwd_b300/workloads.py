@@ -79,7 +79,7 @@ def prefill_inputs(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int,
 
 @dataclasses.dataclass
 class PagedBatch:
-    q: torch.Tensor               # [S, H, d] bf16
+    q: torch.Tensor               # [S, H, d] bf16 (decode) or [S, H, Nq, d] (chunked prefill)
     k_cache: torch.Tensor         # [num_blocks, Hkv, block_size, d] bf16 (NaN-poisoned spares)
     v_cache: torch.Tensor
     block_table: torch.Tensor     # [S, max_blocks_per_seq] int32
@@ -131,7 +131,7 @@ def paged_decode_inputs(num_seqs: int = 64, H: int = 32, Hkv: int = 8, d: int = 
                         max_blocks_per_seq: Optional[int] = None, seed: int = 0,
                         perm_seed: Optional[int] = None, share: bool = True,
                         index_probe: bool = False):
-    """Build a paged KV cache batch (see module docstring for the recipe).
+    """Build a paged KV cache batch for decode (see module docstring for the recipe).
 
     ``perm_seed``: draw the physical permutation from its own generator (all
     other draws unchanged), so tests can vary only the block placement.
@@ -143,16 +143,51 @@ def paged_decode_inputs(num_seqs: int = 64, H: int = 32, Hkv: int = 8, d: int = 
     (v[..., 0] = 1 + t // 64, v[..., 1] = 1 + t % 64, v[..., 2] = 1 + kv head;
     never 0, so the ~1e-16 weight of the other keys cannot show after rounding).
     """
+    g = torch.Generator("cpu").manual_seed(seed)
+    q = torch.randn(num_seqs, H, d, generator=g, dtype=torch.float32)
+    lens = torch.randint(min_len, max_len + 1, (num_seqs,), generator=g, dtype=torch.int64)
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = (max_len + block_size - 1) // block_size
+    return _paged_pool(g, q, lens, H, Hkv, d, block_size, group, shared_tokens, spare_frac,
+                       max_blocks_per_seq, perm_seed, share, index_probe)
+
+
+def paged_prefill_inputs(num_seqs: int = 8, H: int = 32, Hkv: int = 8, d: int = 128,
+                         Nq: int = 2048, block_size: int = 16, min_hist: int = 0,
+                         max_hist: int = 14336, group: int = 1, shared_tokens: int = 0,
+                         spare_frac: float = 0.05, qk_gain: float = 1.0,
+                         max_blocks_per_seq: Optional[int] = None, seed: int = 0,
+                         perm_seed: Optional[int] = None, share: bool = True):
+    """Paged KV cache for a chunked prefill: every sequence appends a chunk of
+    ``Nq`` new tokens to a cached history of U{min_hist..max_hist} tokens.
+
+    The cache already holds the chunk's own K/V, so sequence s has
+    ``seq_lens[s] = hist_s + Nq`` cached tokens.  q is [S, H, Nq, d].  Draw
+    order: Q, history lengths, then the pool exactly as for decode.
+    ``qk_gain`` scales Q and every K block in float32 before rounding.
+    """
+    g = torch.Generator("cpu").manual_seed(seed)
+    q = torch.randn(num_seqs, H, Nq, d, generator=g, dtype=torch.float32)
+    hist = torch.randint(min_hist, max_hist + 1, (num_seqs,), generator=g, dtype=torch.int64)
+    lens = hist + Nq
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = (max_hist + Nq + block_size - 1) // block_size
+    if qk_gain != 1.0:
+        q.mul_(qk_gain)
+    return _paged_pool(g, q, lens, H, Hkv, d, block_size, group, shared_tokens, spare_frac,
+                       max_blocks_per_seq, perm_seed, share, False, k_gain=qk_gain)
+
+
+def _paged_pool(g, q, lens, H, Hkv, d, block_size, group, shared_tokens, spare_frac,
+                max_blocks_per_seq, perm_seed, share, index_probe, k_gain: float = 1.0):
+    """Lay the logical blocks of every sequence out in a permuted, NaN-poisoned pool."""
+    num_seqs = q.shape[0]
+    min_len = int(lens.min())
     if group > 1 and shared_tokens % block_size:
         raise ValueError("shared_tokens must be a whole number of blocks")
     if group > 1 and min_len <= shared_tokens:
         raise ValueError("every sequence needs at least one private block")
-    g = torch.Generator("cpu").manual_seed(seed)
-    q = torch.randn(num_seqs, H, d, generator=g, dtype=torch.float32)
-    lens = torch.randint(min_len, max_len + 1, (num_seqs,), generator=g, dtype=torch.int64)
     nblk = [(int(n) + block_size - 1) // block_size for n in lens]
-    if max_blocks_per_seq is None:
-        max_blocks_per_seq = (max_len + block_size - 1) // block_size
     if max(nblk) > max_blocks_per_seq:
         raise ValueError("max_blocks_per_seq too small")
     shared_blocks = shared_tokens // block_size if group > 1 else 0
@@ -194,6 +229,8 @@ def paged_decode_inputs(num_seqs: int = 64, H: int = 32, Hkv: int = 8, d: int = 
     src = torch.tensor([draw_of[prefix_src.get(u, u)] for u in range(U)], dtype=torch.long)
     k_u = kd[src]
     v_u = vd[src]
+    if k_gain != 1.0:
+        k_u.mul_(k_gain)
     if index_probe:
         k_u, v_u, q = _index_probe(q, k_u, v_u, logical_ids, lens, block_size, H, Hkv, d, g,
                                    shared_blocks)

@@ -16,8 +16,9 @@ Modules
                and P materialised, plus the per-row log-sum-exp; and a
                chunked online-softmax restatement of the single-pass
                recurrence, used only to pin the definition.
-``paged``      paged-decode reference: gathers each sequence's logical K/V
-               through the block table, then applies the definition.
+``paged``      paged-decode and chunked paged-prefill references: gather
+               each sequence's logical K/V through the block table, then
+               apply the definition.
 ``bf16``       exact decoding of bfloat16 bit patterns to float64.
 
 Every function states the passage of the source pages it follows.  Every
@@ -34,7 +35,7 @@ from .attention import (
     attention_ref,
     attention_online,
 )
-from .paged import gather_logical_kv, paged_decode_ref, paged_decode_ref_from_pool
+from .paged import gather_logical_kv, paged_decode_ref, paged_decode_ref_from_pool, paged_prefill_ref
 
 __all__ = [
     "bf16_bits_to_f64",
@@ -46,4 +47,5 @@ __all__ = [
     "gather_logical_kv",
     "paged_decode_ref",
     "paged_decode_ref_from_pool",
+    "paged_prefill_ref",
 ]

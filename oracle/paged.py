@@ -24,6 +24,9 @@ Two entry points:
 * ``paged_decode_ref`` takes each sequence's LOGICAL contiguous K/V and never
   sees a block table.  The GPU parity tests compare against this one, so an
   indexing error on the GPU cannot be cancelled by the same error here.
+* ``paged_prefill_ref`` is the chunked-prefill case: each sequence's Nq new
+  queries attend its logical K/V (the cache already holds the chunk's own
+  keys), with the causal mask aligned to the end of the cache.
 * ``paged_decode_ref_from_pool`` first gathers the logical K/V from a
   physical pool through the block table (``gather_logical_kv``, plain loops),
   then calls the same definition.  Tests pin it to ``paged_decode_ref``
@@ -34,7 +37,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .attention import scores, softmax_rows
+from .attention import attention_ref, scores, softmax_rows
 
 
 def paged_decode_ref(q: np.ndarray, k_seqs, v_seqs, scale: float):
@@ -92,3 +95,35 @@ def paged_decode_ref_from_pool(q, k_cache, v_cache, block_table, seq_lens,
     ks = gather_logical_kv(k_cache, block_table, seq_lens, block_size)
     vs = gather_logical_kv(v_cache, block_table, seq_lens, block_size)
     return paged_decode_ref(q, ks, vs, scale)
+
+
+def paged_prefill_ref(q: np.ndarray, k_seqs, v_seqs, scale: float, causal: bool, rows=None):
+    """Chunked prefill over a paged cache, by the plain definition.
+
+    q: [S, H, Nq, d] float64, the Nq newest tokens of every sequence (the
+    chunk being prefilled).  k_seqs / v_seqs: entry s is sequence s's logical
+    K / V, [seq_len_s, Hkv, d]; the chunk's own keys are its last Nq entries.
+    Returns O [S, H, R, d] and lse [S, H, R] for the query rows ``rows``
+    (default all Nq).
+
+    Tutorial "第 3 章 进阶原理:性能模型与数值稳定性", section 3.0.6: FlashAttention
+    and PagedAttention cooperate -- the fused kernel reads its keys through the
+    block table.  Query row i of the chunk is token seq_len - Nq + i of the
+    sequence, so under the causal mask it attends keys j <= i + (seq_len - Nq)
+    (the bottom-right alignment of ``oracle.attention``); a row with no key
+    (seq_len < Nq) gives O = 0 and lse = -inf.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    S_, H, Nq, d = q.shape
+    R = Nq if rows is None else len(rows)
+    O = np.zeros((S_, H, R, d))
+    lse = np.zeros((S_, H, R))
+    for s in range(S_):
+        ks = np.asarray(k_seqs[s], dtype=np.float64)   # [n, Hkv, d]
+        vs = np.asarray(v_seqs[s], dtype=np.float64)
+        kk = ks.transpose(1, 0, 2)[None]                # [1, Hkv, n, d]
+        vv = vs.transpose(1, 0, 2)[None]
+        Os, Ls = attention_ref(q[s][None], kk, vv, scale, causal, rows=rows)
+        O[s] = Os[0]
+        lse[s] = Ls[0]
+    return O, lse
