@@ -19,6 +19,8 @@ Modules
 ``paged``      paged-decode and chunked paged-prefill references: gather
                each sequence's logical K/V through the block table, then
                apply the definition.
+``backward``   gradients of the definition (dQ, dK, dV) by the chain rule,
+               with P materialised.
 ``bf16``       exact decoding of bfloat16 bit patterns to float64.
 
 Every function states the passage of the source pages it follows.  Every
@@ -35,6 +37,7 @@ from .attention import (
     attention_ref,
     attention_online,
 )
+from .backward import attention_bwd_ref
 from .paged import gather_logical_kv, paged_decode_ref, paged_decode_ref_from_pool, paged_prefill_ref
 
 __all__ = [
@@ -48,4 +51,5 @@ __all__ = [
     "paged_decode_ref",
     "paged_decode_ref_from_pool",
     "paged_prefill_ref",
+    "attention_bwd_ref",
 ]
