@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     AttnError,
     attn_fwd,
     paged_decode,
+    paged_prefill,
     paged_decode_workspace_size,
     library_path,
     load_library,

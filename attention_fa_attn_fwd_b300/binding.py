@@ -40,6 +40,8 @@ SIGNATURES = {
                           _vp, _vp, _vp, _sz, _vp]),
     "paged_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                                   _vp, _vp, _vp]),
+    "paged_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
+                           _vp, _vp, _vp]),
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_device_status": (_i, [_vp]),
 }
@@ -217,6 +219,51 @@ def paged_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
                                   block_table.data_ptr(), seq_lens.data_ptr(), S, H, Hkv, d,
                                   num_blocks, block_table.shape[1], block_size, float(scale),
                                   o.data_ptr(), lse.data_ptr(), _stream_handle(stream))
+    _check(st)
+    return o, lse
+
+
+def paged_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                  block_table: torch.Tensor, seq_lens: torch.Tensor, causal: bool = True,
+                  scale: Optional[float] = None, o: Optional[torch.Tensor] = None,
+                  lse: Optional[torch.Tensor] = None, want_lse: bool = True,
+                  stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunked prefill over a paged KV cache via ``paged_prefill``.
+
+    q [S,H,Nq,d] bf16 (each sequence's newest Nq tokens); k_cache/v_cache
+    [num_blocks,Hkv,16,d] bf16; block_table [S,max_blocks] int32; seq_lens
+    [S] int32 (cached tokens, the chunk included).  Returns
+    (o [S,H,Nq,d] bf16, lse [S,H,Nq] fp32 or None).
+    """
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    S, H, Nq, d = q.shape
+    num_blocks, Hkv, block_size, dk = k_cache.shape
+    if v_cache.shape != k_cache.shape or dk != d:
+        raise ValueError("k_cache / v_cache / q shapes disagree")
+    if block_table.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_table / seq_lens must have num_seqs rows")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _need(o, "o", torch.bfloat16, 4)
+        if o.shape != q.shape:
+            raise ValueError("o must have q's shape")
+    if lse is None and want_lse:
+        lse = torch.empty((S, H, Nq), dtype=torch.float32, device=q.device)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    st = lib.paged_prefill(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                           block_table.data_ptr(), seq_lens.data_ptr(), S, H, Hkv, Nq, d,
+                           num_blocks, block_table.shape[1], block_size, float(scale),
+                           int(bool(causal)), o.data_ptr(),
+                           lse.data_ptr() if lse is not None else None, _stream_handle(stream))
     _check(st)
     return o, lse
 

@@ -143,6 +143,42 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   return ATTN_OK;
 }
 
+attn_status paged_prefill(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_table, const int32_t* seq_lens, int num_seqs, int H,
+                          int Hkv, int Nq, int d, int num_blocks, int max_blocks_per_seq,
+                          int block_size, float scale, int causal, void* o, float* lse,
+                          attn_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o)
+    return fail(ATTN_EINVAL, "paged_prefill: null pointer argument");
+  if (num_seqs < 1 || H < 1 || Hkv < 1 || Nq < 1 || num_blocks < 1 || max_blocks_per_seq < 1)
+    return fail(ATTN_EINVAL, "paged_prefill: sizes must be >= 1");
+  if (H % Hkv != 0) return fail(ATTN_EINVAL, "paged_prefill: H=%d not a multiple of Hkv=%d", H, Hkv);
+  if (block_size != 16) return fail(ATTN_EINVAL, "paged_prefill: block_size must be 16");
+  if (!(scale > 0.f) || !(scale < 3.0e38f))
+    return fail(ATTN_EINVAL, "paged_prefill: scale must be positive and finite");
+  if (causal != 0 && causal != 1) return fail(ATTN_EINVAL, "paged_prefill: causal must be 0 or 1");
+  if (d != 64 && d != 128) return fail(ATTN_EUNSUPPORTED, "paged_prefill: head dim %d", d);
+  if ((long long)num_blocks * Hkv * 16 >= (1LL << 31) - 16)
+    return fail(ATTN_EINVAL, "paged_prefill: KV pool too large for 32-bit row coordinates");
+  if ((long long)max_blocks_per_seq * 16 >= (1LL << 31))
+    return fail(ATTN_EINVAL, "paged_prefill: max_blocks_per_seq too large");
+  if ((long long)num_seqs * H * ((Nq + 255) / 256) >= (1LL << 31))
+    return fail(ATTN_EINVAL, "paged_prefill: problem too large");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)))
+    return fail(ATTN_EINVAL, "paged_prefill: misaligned pointer");
+  attn_status st = check_device();
+  if (st != ATTN_OK) return st;
+  const char* err = nullptr;
+  cudaError_t e = attn::paged_prefill_launch(q, k_cache, v_cache, block_table, seq_lens, num_seqs,
+                                             H, Hkv, Nq, d, num_blocks, max_blocks_per_seq, scale,
+                                             causal, o, lse, reinterpret_cast<cudaStream_t>(stream),
+                                             &err);
+  if (err) return fail(ATTN_ECUDA, "paged_prefill: %s", err);
+  if (e != cudaSuccess) return fail(ATTN_ECUDA, "paged_prefill launch: %s", cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
 size_t paged_decode_workspace_size(int num_seqs, int H, int Hkv, int d, int max_blocks_per_seq) {
   if (num_seqs < 1 || H < 1 || Hkv < 1 || H % Hkv || max_blocks_per_seq < 1 || (d != 64 && d != 128))
     return 0;

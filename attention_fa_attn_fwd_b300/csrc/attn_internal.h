@@ -18,6 +18,11 @@ int prefill_smem_bytes(int d);
 cudaError_t prefill_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                            int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
                            cudaStream_t stream, const char** err);
+cudaError_t paged_prefill_launch(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_table, const int32_t* kv_lens, int B, int H,
+                                 int Hkv, int Nq, int d, int num_blocks, int max_blocks,
+                                 float scale, int causal, void* o, float* lse,
+                                 cudaStream_t stream, const char** err);
 int prefill_take_device_error();  // reads and clears (synchronous)
 
 // ---- paged decode (decode_sm103.cu)

@@ -27,6 +27,18 @@
 //               normalisation), bf16 O through smem and a TMA store,
 //               lse = (m + log2 l) ln 2.
 //
+// Paged variant (kPaged): K and V are read through a PagedAttention block
+// table instead of from contiguous [B, Hkv, Nk, d] tensors (tutorial
+// "第 3 章 进阶原理:性能模型与数值稳定性", section 3.0.6: the fused kernel and the
+// paged cache work together).  Sequence b has kv_lens[b] cached tokens, the
+// last Nq of which are the queries' own; a 128-key tile is 8 blocks of 16
+// tokens, each fetched by its own 16-row TMA box into the same swizzled
+// layout one 128-row box would produce.  Blocks past the sequence end are
+// fetched from an out-of-range row (TMA fills zeros); cache slots past the
+// end inside the last block may hold anything, so the MMA warp zeroes those V
+// rows in shared memory before the first P V that reads them (K needs no
+// fix-up: the mask replaces those scores).
+//
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d);
 // P_i occupies the first 64 columns of S_i.  tcgen05.mma operations of one
 // issuing thread execute in order, so QK(i,j+1) overwriting P_i happens after
@@ -95,9 +107,16 @@ struct Args {
   int n_pairs;   // ceil(Nq / 256)
   float c_log2;  // scale * log2(e)
   int causal;
+  // paged variant only
+  const int32_t* block_table;  // [B, max_blocks]
+  const int32_t* kv_lens;      // [B]
+  int max_blocks, num_blocks;
+  int oob_row;                 // a pool row past the end: TMA fills zeros
 };
 
-template <int D>
+constexpr int kPageTokens = 16;  // PagedAttention block size
+
+template <int D, bool kPaged>
 __global__ void __launch_bounds__(384, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -122,15 +141,28 @@ __global__ void __launch_bounds__(384, 1)
   const int q0 = (a.n_pairs - 1 - int(blockIdx.x / BH)) * 256;
   const int b = bh / a.H;
   const int h = bh % a.H;
-  const int zkv = b * a.Hkv + h / (a.H / a.Hkv);
+  const int g_kv = h / (a.H / a.Hkv);
+  const int zkv = b * a.Hkv + g_kv;
   const bool dead = timed_out_before(err);
+  // Keys of this sequence; the paged variant reads its own length.
+  int Nk = a.Nk;
+  int nblk = 0;  // paged: cached blocks of this sequence
+  if constexpr (kPaged) {
+    Nk = a.kv_lens[b];
+    if (Nk < 0 || Nk > a.max_blocks * kPageTokens) {
+      if (threadIdx.x == 0 && q0 == (a.n_pairs - 1) * 256 && h == 0)
+        atomicCAS(err, 0, kErrPagedBadLength);
+      Nk = min(max(Nk, 0), a.max_blocks * kPageTokens);
+    }
+    nblk = (Nk + kPageTokens - 1) / kPageTokens;
+  }
   // KV tiles each Q tile attends (0 for a tile past Nq or fully masked).
   int n_t[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int r0 = q0 + i * 128;
-    int kv_end = a.Nk;
-    if (a.causal) kv_end = min(a.Nk, r0 + 128 + (a.Nk - a.Nq));
+    int kv_end = Nk;
+    if (a.causal) kv_end = min(Nk, r0 + 128 + (Nk - a.Nq));
     n_t[i] = (r0 < a.Nq && kv_end > 0 && !dead) ? (kv_end + 127) / 128 : 0;
   }
   const int n_kv = max(n_t[0], n_t[1]);
@@ -178,25 +210,49 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_3d_elect(sbase + C::kOffQ + i * C::kTileBytes + s * C::kSlabBytes, &tm_q,
                               bar(C::kBarQF + i), s * 64, q0 + i * 128, bh);
         }
+        // One K or V tile: a single 128-row box per slab, or (paged) lanes
+        // 0..7 each fetch one 16-token block per slab at pool row `prow`.
+        auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t fb, int j, int prow) {
+          if constexpr (!kPaged) {
+            for (int s = 0; s < C::kSlabs; ++s)
+              tma_load_3d_elect(dst + s * C::kSlabBytes, tm, fb, s * 64, j * 128, zkv);
+          } else {
+            __syncwarp();
+            if (lane < 8)
+              for (int s = 0; s < C::kSlabs; ++s)
+                tma_load_3d(dst + s * C::kSlabBytes + lane * (kPageTokens * 128), tm, fb, s * 64,
+                            prow, 0);
+          }
+        };
+        const int32_t* bt = nullptr;
+        if constexpr (kPaged) bt = a.block_table + size_t(b) * a.max_blocks;
         for (int j = 0; j < n_kv; ++j) {
           const int ks = j % C::kKStages, vs = j % C::kVStages;
+          int prow = 0;
+          if constexpr (kPaged) {
+            prow = a.oob_row;
+            const int lb = j * 8 + lane;
+            if (lane < 8 && lb < nblk) {
+              const int phys = bt[lb];
+              if (phys >= 0 && phys < a.num_blocks)
+                prow = (phys * a.Hkv + g_kv) * kPageTokens;
+              else
+                atomicCAS(err, 0, kErrPagedBadBlock);
+            }
+          }
           ok = __all_sync(0xffffffffu,
                           mbar_wait(bar(C::kBarKE + ks), ((j / C::kKStages) & 1) ^ 1, abort_flag,
                                     err, kErrTimeoutProducer));
           if (!ok) break;
           mbar_arrive_expect_tx_elect(bar(C::kBarKF + ks), C::kTileBytes);
-          for (int s = 0; s < C::kSlabs; ++s)
-            tma_load_3d_elect(sbase + C::kOffK + ks * C::kTileBytes + s * C::kSlabBytes, &tm_k,
-                              bar(C::kBarKF + ks), s * 64, j * 128, zkv);
+          load_tile(&tm_k, sbase + C::kOffK + ks * C::kTileBytes, bar(C::kBarKF + ks), j, prow);
           k_issued = j + 1;
           ok = __all_sync(0xffffffffu,
                           mbar_wait(bar(C::kBarVE + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag,
                                     err, kErrTimeoutProducer));
           if (!ok) break;
           mbar_arrive_expect_tx_elect(bar(C::kBarVF + vs), C::kTileBytes);
-          for (int s = 0; s < C::kSlabs; ++s)
-            tma_load_3d_elect(sbase + C::kOffV + vs * C::kTileBytes + s * C::kSlabBytes, &tm_v,
-                              bar(C::kBarVF + vs), s * 64, j * 128, zkv);
+          load_tile(&tm_v, sbase + C::kOffV + vs * C::kTileBytes, bar(C::kBarVF + vs), j, prow);
           v_issued = j + 1;
         }
         if (!ok) {
@@ -243,6 +299,16 @@ __global__ void __launch_bounds__(384, 1)
           if (i == 1 || j >= n_t[1]) mma_commit(bar(C::kBarKE + ks));
           return true;
         };
+        // Paged: the V tile holding the sequence's partial last block, and
+        // the rows of that block past the end (garbage in the cache).
+        int tail_tile = -1, tail_r0 = 0, tail_r1 = 0;
+        if constexpr (kPaged) {
+          if (Nk % kPageTokens != 0) {
+            tail_tile = (Nk - 1) / 128;
+            tail_r0 = Nk - tail_tile * 128;
+            tail_r1 = min(128, nblk * kPageTokens - tail_tile * 128);
+          }
+        }
         // O_i += P_i V_j, P_i read from the first 64 TMEM columns of S_i.
         auto issue_pv = [&](int i, int j) -> bool {
           const int vs = j % C::kVStages;
@@ -252,6 +318,22 @@ __global__ void __launch_bounds__(384, 1)
           if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarVF + vs), (j / C::kVStages) & 1,
                                                  abort_flag, err, kErrTimeoutMma)))
             return false;
+          if constexpr (kPaged) {
+            if (j == tail_tile) {
+              // 0-probability keys must contribute exactly 0: clear the rows
+              // past the end once, before the first MMA that reads them.
+              const int nr = tail_r1 - tail_r0;
+              uint8_t* vt = smem + C::kOffV + vs * C::kTileBytes;
+              for (int idx = lane; idx < C::kSlabs * nr * 8; idx += 32) {
+                const int sl = idx / (nr * 8), rem = idx % (nr * 8);
+                *reinterpret_cast<uint4*>(vt + sl * C::kSlabBytes + (tail_r0 + rem / 8) * 128 +
+                                          (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              tail_tile = -1;
+            }
+          }
           tc_fence_after();
           const uint32_t a_tmem = tmem + C::kColS + i * 128;
           const uint64_t vo = uint64_t((vs * C::kTileBytes) >> 4);
@@ -298,7 +380,7 @@ __global__ void __launch_bounds__(384, 1)
     const int n = n_t[wg];
     const int q_row = q0 + wg * 128 + row;
     // Last key this row may attend (bottom-right causal alignment).
-    const int row_last = a.causal ? min(a.Nk - 1, q_row + (a.Nk - a.Nq)) : (a.Nk - 1);
+    const int row_last = a.causal ? min(Nk - 1, q_row + (Nk - a.Nq)) : (Nk - 1);
     const float c = a.c_log2;
     float m = -INFINITY;  // reference maximum, log2 units of the scaled score
     float l = 0.f;        // running sum of 2^(s*c - m)
@@ -446,6 +528,33 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// Sets the kernel's dynamic shared memory limit once per device and variant.
+template <int D, bool kPaged>
+cudaError_t configure_once() {
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(prefill_fwd_kernel<D, kPaged>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  return cudaSuccess;
+}
+
+// Q and O: [B*H, Nq, D] viewed as a 3-D tensor (D, Nq, B*H), 64 x 128 boxes.
+template <int D>
+bool encode_q_o(CUtensorMap* tq, CUtensorMap* to, const void* q, void* o, int B, int H, int Nq,
+                const char** err) {
+  const uint32_t box[3] = {64, 128, 1};
+  const uint64_t dq[3] = {uint64_t(D), uint64_t(Nq), uint64_t(B) * H};
+  const uint64_t sq[2] = {uint64_t(D) * 2, uint64_t(Nq) * D * 2};
+  return encode_tmap_bf16(tq, q, 3, dq, sq, box, true, err) &&
+         encode_tmap_bf16(to, o, 3, dq, sq, box, true, err);
+}
+
 template <int D>
 cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                    int Hkv, int Nq, int Nk, float scale, int causal, cudaStream_t stream,
@@ -453,25 +562,14 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
   using C = Cfg<D>;
   CUtensorMap tq, tk, tv, to;
   const uint32_t box[3] = {64, 128, 1};
-  const uint64_t dq[3] = {uint64_t(D), uint64_t(Nq), uint64_t(B) * H};
-  const uint64_t sq[2] = {uint64_t(D) * 2, uint64_t(Nq) * D * 2};
   const uint64_t dk[3] = {uint64_t(D), uint64_t(Nk), uint64_t(B) * Hkv};
   const uint64_t sk[2] = {uint64_t(D) * 2, uint64_t(Nk) * D * 2};
-  if (!encode_tmap_bf16(&tq, q, 3, dq, sq, box, true, err)) return cudaErrorInvalidValue;
+  if (!encode_q_o<D>(&tq, &to, q, o, B, H, Nq, err)) return cudaErrorInvalidValue;
   if (!encode_tmap_bf16(&tk, k, 3, dk, sk, box, true, err)) return cudaErrorInvalidValue;
   if (!encode_tmap_bf16(&tv, v, 3, dk, sk, box, true, err)) return cudaErrorInvalidValue;
-  if (!encode_tmap_bf16(&to, o, 3, dq, sq, box, true, err)) return cudaErrorInvalidValue;
-  static thread_local int configured_device[2] = {-1, -1};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = configure_once<D, false>();
   if (e != cudaSuccess) return e;
-  if (configured_device[D == 128] != dev) {
-    e = cudaFuncSetAttribute(prefill_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured_device[D == 128] = dev;
-  }
-  Args a;
+  Args a = {};
   a.lse = lse;
   a.B = B;
   a.H = H;
@@ -482,7 +580,45 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
   a.c_log2 = scale * kLog2e;
   a.causal = causal;
   const unsigned grid = unsigned(a.n_pairs) * unsigned(B) * unsigned(H);
-  prefill_fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
+  prefill_fwd_kernel<D, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_paged(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_table, const int32_t* kv_lens, int B, int H, int Hkv,
+                         int Nq, int num_blocks, int max_blocks, float scale, int causal, void* o,
+                         float* lse, cudaStream_t stream, const char** err) {
+  using C = Cfg<D>;
+  CUtensorMap tq, tk, tv, to;
+  // The pool [num_blocks, Hkv, 16, D] as rows of D: one (block, KV head) is
+  // 16 consecutive rows, fetched by one 64 x 16 box per 64-column slab.
+  const uint64_t rows = uint64_t(num_blocks) * Hkv * kPageTokens;
+  const uint32_t box[3] = {64, uint32_t(kPageTokens), 1};
+  const uint64_t dk[3] = {uint64_t(D), rows, 1};
+  const uint64_t sk[2] = {uint64_t(D) * 2, rows * D * 2};
+  if (!encode_q_o<D>(&tq, &to, q, o, B, H, Nq, err)) return cudaErrorInvalidValue;
+  if (!encode_tmap_bf16(&tk, k_cache, 3, dk, sk, box, true, err)) return cudaErrorInvalidValue;
+  if (!encode_tmap_bf16(&tv, v_cache, 3, dk, sk, box, true, err)) return cudaErrorInvalidValue;
+  cudaError_t e = configure_once<D, true>();
+  if (e != cudaSuccess) return e;
+  Args a = {};
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.Nq = Nq;
+  a.Nk = 0;
+  a.n_pairs = (Nq + 255) / 256;
+  a.c_log2 = scale * kLog2e;
+  a.causal = causal;
+  a.block_table = block_table;
+  a.kv_lens = kv_lens;
+  a.max_blocks = max_blocks;
+  a.num_blocks = num_blocks;
+  a.oob_row = int(rows);
+  const unsigned grid = unsigned(a.n_pairs) * unsigned(B) * unsigned(H);
+  prefill_fwd_kernel<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 
@@ -495,6 +631,18 @@ cudaError_t prefill_launch(const void* q, const void* k, const void* v, void* o,
                            cudaStream_t stream, const char** err) {
   if (d == 128) return launch<128>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, stream, err);
   return launch<64>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, stream, err);
+}
+
+cudaError_t paged_prefill_launch(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_table, const int32_t* kv_lens, int B, int H,
+                                 int Hkv, int Nq, int d, int num_blocks, int max_blocks,
+                                 float scale, int causal, void* o, float* lse,
+                                 cudaStream_t stream, const char** err) {
+  if (d == 128)
+    return launch_paged<128>(q, k_cache, v_cache, block_table, kv_lens, B, H, Hkv, Nq, num_blocks,
+                             max_blocks, scale, causal, o, lse, stream, err);
+  return launch_paged<64>(q, k_cache, v_cache, block_table, kv_lens, B, H, Hkv, Nq, num_blocks,
+                          max_blocks, scale, causal, o, lse, stream, err);
 }
 
 int prefill_take_device_error() {

@@ -21,6 +21,8 @@ enum : int {
   kErrTimeoutSoftmax = 0x103,
   kErrTimeoutEpilogue = 0x104,
   kErrDecodeBadBlock = 0x201,
+  kErrPagedBadBlock = 0x202,   // paged prefill: block id outside [0, num_blocks)
+  kErrPagedBadLength = 0x203,  // paged prefill: kv_lens[b] < 0 or > 16 * max_blocks
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

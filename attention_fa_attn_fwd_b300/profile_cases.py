@@ -3,10 +3,12 @@
     python -m attention_fa_attn_fwd_b300.profile_cases --case prefill --iters 3
     python -m attention_fa_attn_fwd_b300.profile_cases --case decode --iters 3
     python -m attention_fa_attn_fwd_b300.profile_cases --case step --iters 3
+    python -m attention_fa_attn_fwd_b300.profile_cases --case paged_prefill --iters 3
 
 ``prefill``: attn_fwd on the long-context causal GQA workload (B1 H32 Hkv8
 N16384 d128; 335 MB on the device, larger than L2).  ``decode``: paged_decode
 on the 64-sequence workload (2.3 GB pool).  ``step``: both, as one bench step.
+``paged_prefill``: chunked prefill of 8 x 2048 tokens over a paged cache.
 A 256 MiB L2 flush (a memset, not one of this library's kernels) precedes
 every kernel, as in bench.py.  Prints the CUDA-event time of each launch.
 """
@@ -23,7 +25,7 @@ from . import binding, workloads
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=["prefill", "decode", "step"], default="step")
+    ap.add_argument("--case", choices=["prefill", "decode", "step", "paged_prefill"], default="step")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--prefill", default="gqa_b1h32kv8_n16384_d128_causal")
     ap.add_argument("--decode-seqs", type=int, default=64,
@@ -52,6 +54,15 @@ def main(argv=None):
         ws = torch.empty(n, dtype=torch.uint8, device=dev)
         runs.append(("paged_decode", lambda: binding.paged_decode(dq, kc, vc, bt, sl, o=do, lse=dl,
                                                                   workspace=ws)))
+    if args.case == "paged_prefill":
+        pcfg = workloads.PAGED_PREFILL_WORKLOADS["paged_prefill_s8_h32kv8_q2048_d128"]
+        pp = workloads.paged_prefill_inputs(**pcfg)
+        pq, pkc, pvc = pp.q.to(dev), pp.k_cache.to(dev), pp.v_cache.to(dev)
+        pbt, psl = pp.block_table.to(dev), pp.seq_lens.to(dev)
+        po = torch.empty_like(pq)
+        pl = torch.empty(pq.shape[:3], dtype=torch.float32, device=dev)
+        runs.append(("paged_prefill", lambda: binding.paged_prefill(pq, pkc, pvc, pbt, psl,
+                                                                    o=po, lse=pl)))
     for it in range(args.iters):
         for name, fn in runs:
             flush.zero_()

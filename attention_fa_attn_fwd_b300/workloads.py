@@ -64,6 +64,15 @@ PAGED_WORKLOADS = {
 }
 
 
+# Chunked prefill over a paged cache: 8 sequences each append a 2048-token
+# chunk to a history of U{0..14336} cached tokens (at most 16384 in all).
+PAGED_PREFILL_WORKLOADS = {
+    "paged_prefill_s8_h32kv8_q2048_d128": dict(num_seqs=8, H=32, Hkv=8, d=128, Nq=2048,
+                                              block_size=16, min_hist=0, max_hist=14336,
+                                              group=1, shared_tokens=0, spare_frac=0.05),
+}
+
+
 def prefill_inputs(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int,
                    seed: int = 0, qk_gain: float = 1.0, **_unused):
     """Q [B,H,Nq,d], K [B,Hkv,Nk,d], V [B,Hkv,Nk,d] bfloat16 on the CPU."""

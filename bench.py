@@ -41,6 +41,7 @@ from attention_fa_attn_fwd_b300 import workloads  # noqa: E402
 
 PREFILL = "gqa_b1h32kv8_n16384_d128_causal"
 DECODE = "paged_decode_s64_h32kv8_d128"
+PAGED_PREFILL = "paged_prefill_s8_h32kv8_q2048_d128"
 METRIC = "prefill attn TFLOP/s & % BF16 tensor peak; paged decode KV GB/s & % HBM"
 FLUSH_BYTES = 256 << 20
 
@@ -60,6 +61,19 @@ def load_peaks():
 def prefill_flops(cfg) -> float:
     f = 4.0 * cfg["B"] * cfg["H"] * cfg["Nq"] * cfg["Nk"] * cfg["d"]
     return f / 2 if cfg["causal"] else f
+
+
+def paged_prefill_flops(seq_lens, H: int, Nq: int, d: int, causal: bool = True) -> float:
+    """4*H*d FLOPs per (query, unmasked key) pair; query i of a chunk of Nq in a
+    cache of n tokens sees min(n, i + n - Nq + 1) keys under the causal mask."""
+    pairs = 0
+    for n in (int(x) for x in seq_lens):
+        if not causal:
+            pairs += Nq * n
+            continue
+        for i in range(Nq):
+            pairs += max(0, min(n, i + n - Nq + 1))
+    return 4.0 * H * d * pairs
 
 
 def source_hash(files):
@@ -340,6 +354,34 @@ def run_ours(args, ws, rank, local):
     small_bytes = (dq.numel() * 2 * 2 + bt.numel() * 4 + sl.numel() * 4 + dlse.numel() * 4)
     dec_gbs = ws * (uniq_bytes + small_bytes) / (d_mean * 1e-3) / 1e9
 
+    # ---- chunked prefill over the paged cache (reported beside the step)
+    ppc = workloads.PAGED_PREFILL_WORKLOADS[PAGED_PREFILL]
+    pp = workloads.paged_prefill_inputs(**ppc, seed=rank)
+    pq, pkc, pvc = pp.q.to(dev), pp.k_cache.to(dev), pp.v_cache.to(dev)
+    pbt, psl = pp.block_table.to(dev), pp.seq_lens.to(dev)
+    po = torch.empty_like(pq)
+    plse = torch.empty(pq.shape[:3], dtype=torch.float32, device=dev)
+
+    def paged_prefill():
+        binding.paged_prefill(pq, pkc, pvc, pbt, psl, causal=True, o=po, lse=plse, stream=stream)
+
+    for _ in range(3):
+        flush.zero_()
+        paged_prefill()
+    Kp = max(3, min(K, 100))
+    p_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kp)]
+    for i in range(Kp):
+        flush.zero_()
+        p_evs[i][0].record(stream)
+        paged_prefill()
+        p_evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert binding.device_status(stream) == 0
+    pp_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in p_evs), ws)
+    pp_flops = paged_prefill_flops(pp.seq_lens, ppc["H"], ppc["Nq"], ppc["d"]) * ws
+    pp_tflops = pp_flops / (pp_ms * 1e-3) / 1e12
+    del pq, pkc, pvc, pbt, psl, po, plse
+
     # ---- end to end through the public API with pinned host buffers
     qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
     op = torch.empty(q_h.shape, dtype=torch.bfloat16).pin_memory()
@@ -410,6 +452,10 @@ def run_ours(args, ws, rank, local):
                             "unit": "GB/s", "frac": k_gbs / peaks["hbm_gbs"],
                             "traffic": committed_traffic("decode_split_kernel", ["decode_sm103.cu", "ptx.cuh"]),
                             "kernel": "decode_split_kernel<128> + decode_merge_kernel<128>"},
+        "paged_prefill": {"workload": PAGED_PREFILL, "config": ppc, "ms": pp_ms,
+                          "tflops": pp_tflops, "frac_burst": pp_tflops / ws / peak_tf,
+                          "flops": pp_flops / ws, "kernel": "prefill_fwd_kernel<128, paged>",
+                          "kv_lens": [int(x) for x in pp.seq_lens]},
         "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "prefill_ms": ep, "decode_ms": ed,
                 "decode_gbs": ws * (uniq_bytes + small_bytes) / (ed * 1e-3) / 1e9},

@@ -149,6 +149,43 @@ ATTN_API attn_status paged_decode_noalloc(const void* q, const void* k_cache, co
                                           int max_blocks_per_seq, int block_size, float scale,
                                           void* o, float* lse, attn_stream_t stream);
 
+/*
+ * paged_prefill -- chunked prefill over a paged KV cache: each sequence's Nq
+ * newest tokens (the chunk being prefilled) attend the sequence's cached keys,
+ * read through the block table, with the same tiled single-pass kernel as
+ * attn_fwd.
+ *
+ * Defined by: tutorial "第 3 章 进阶原理:性能模型与数值稳定性", section 3.0.6
+ * (FlashAttention-2 and PagedAttention used together: the fused kernel reads
+ * the paged cache) and the definition of attn_fwd.
+ *
+ *   q            [num_seqs, H, Nq, d]                  bf16: the chunk's queries
+ *   k_cache      [num_blocks, Hkv, block_size, d]      bf16 pool (as paged_decode)
+ *   v_cache      [num_blocks, Hkv, block_size, d]      bf16
+ *   block_table  [num_seqs, max_blocks_per_seq]        int32 (as paged_decode)
+ *   seq_lens     [num_seqs]                            int32: cached tokens of each
+ *                sequence, the chunk's own keys included (its last Nq tokens).
+ *   o            [num_seqs, H, Nq, d]                  bf16 output
+ *   lse          [num_seqs, H, Nq]                     fp32 output or NULL
+ *   causal 1: query row i is token seq_lens[s] - Nq + i and attends key j iff
+ *          j <= i + seq_lens[s] - Nq (rows with no key: o = 0, lse = -inf);
+ *          0: every cached key.
+ *
+ * Cache slots past a sequence's length may hold any bits (even NaN).  A
+ * block_table entry outside [0, num_blocks) is read as zeros and a seq_lens
+ * entry outside [0, 16 * max_blocks_per_seq] is clamped; both are recorded as
+ * device errors (attn_device_status).
+ *
+ * Requirements: block_size == 16; H % Hkv == 0; d in {64, 128};
+ * num_blocks * Hkv * 16 < 2^31 - 16; pointers 16-byte aligned (block_table,
+ * seq_lens and lse: 4-byte aligned).  No workspace; nothing is allocated.
+ */
+ATTN_API attn_status paged_prefill(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_table, const int32_t* seq_lens,
+                                   int num_seqs, int H, int Hkv, int Nq, int d, int num_blocks,
+                                   int max_blocks_per_seq, int block_size, float scale, int causal,
+                                   void* o, float* lse, attn_stream_t stream);
+
 /* Message for the last non-OK status returned on the calling thread. */
 ATTN_API const char* attn_last_error(void);
 

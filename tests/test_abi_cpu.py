@@ -28,7 +28,7 @@ def lib():
 
 def test_header_declares_expected_api():
     assert declared_functions() == sorted(["attn_fwd", "paged_decode", "paged_decode_workspace_size",
-                                           "paged_decode_noalloc", "attn_last_error",
+                                           "paged_decode_noalloc", "paged_prefill", "attn_last_error",
                                            "attn_device_status"])
 
 
@@ -111,3 +111,32 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _fwd(lib) in (binding.ATTN_ECUDA, binding.ATTN_EUNSUPPORTED)
+
+
+def _pp(lib, **kw):
+    a = dict(q=_fake(1), kc=_fake(2), vc=_fake(3), bt=_fake(4), sl=_fake(5), S=4, H=32, Hkv=8,
+             Nq=256, d=128, nb=100, mb=64, bs=16, scale=0.088, causal=1, o=_fake(6), lse=None,
+             stream=None)
+    a.update(kw)
+    return lib.paged_prefill(a["q"], a["kc"], a["vc"], a["bt"], a["sl"], a["S"], a["H"], a["Hkv"],
+                             a["Nq"], a["d"], a["nb"], a["mb"], a["bs"], a["scale"], a["causal"],
+                             a["o"], a["lse"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), binding.ATTN_EINVAL),
+    (dict(sl=None), binding.ATTN_EINVAL),
+    (dict(S=0), binding.ATTN_EINVAL),
+    (dict(Nq=0), binding.ATTN_EINVAL),
+    (dict(bs=8), binding.ATTN_EINVAL),
+    (dict(H=30), binding.ATTN_EINVAL),
+    (dict(d=96), binding.ATTN_EUNSUPPORTED),
+    (dict(causal=3), binding.ATTN_EINVAL),
+    (dict(scale=float("nan")), binding.ATTN_EINVAL),
+    (dict(nb=1 << 30), binding.ATTN_EINVAL),
+    (dict(o=ctypes.c_void_p(0x10008)), binding.ATTN_EINVAL),
+    (dict(bt=ctypes.c_void_p(0x10002)), binding.ATTN_EINVAL),
+])
+def test_paged_prefill_rejects_bad_arguments(lib, kw, status):
+    assert _pp(lib, **kw) == status
+    assert lib.attn_last_error()
