@@ -7,6 +7,7 @@ tensors to that ABI.  ``workloads`` draws the seeded synthetic inputs.
 
 from .binding import (  # noqa: F401
     AttnError,
+    attn_bwd,
     attn_fwd,
     paged_decode,
     paged_prefill,

@@ -42,6 +42,9 @@ SIGNATURES = {
                                   _vp, _vp, _vp]),
     "paged_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
                            _vp, _vp, _vp]),
+    "attn_bwd_workspace_size": (_sz, [_i, _i, _i]),
+    "attn_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i,
+                      _vp, _sz, _vp]),
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_device_status": (_i, [_vp]),
 }
@@ -136,6 +139,52 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                       _stream_handle(stream))
     _check(st)
     return o, lse
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+             do: torch.Tensor, lse: torch.Tensor, causal: bool = False,
+             scale: Optional[float] = None, dq: Optional[torch.Tensor] = None,
+             dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None, stream=None):
+    """Gradients (dq, dk, dv) of ``attn_fwd`` via ``attn_bwd``.
+
+    q, o, do [B,H,Nq,d] bf16; k, v [B,Hkv,Nk,d] bf16; lse [B,H,Nq] fp32 from
+    ``attn_fwd``.  ``workspace``: uint8 CUDA tensor of at least
+    ``attn_bwd_workspace_size`` bytes (allocated here if omitted).
+    """
+    lib = load_library()
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _need(t, name, torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    B, H, Nq, d = q.shape
+    _, Hkv, Nk, _ = k.shape
+    if k.shape != v.shape or o.shape != q.shape or do.shape != q.shape or k.shape[0] != B \
+            or k.shape[3] != d or tuple(lse.shape) != (B, H, Nq):
+        raise ValueError("attn_bwd: shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, name, ref in ((dq, "dq", q), (dk, "dk", k), (dv, "dv", v)):
+        _need(t, name, torch.bfloat16, 4)
+        if t.shape != ref.shape:
+            raise ValueError(f"{name} has the wrong shape")
+    need = int(lib.attn_bwd_workspace_size(B, H, Nq))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    elif workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise TypeError("workspace must be a uint8 CUDA tensor")
+    st = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                      lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                      B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                      workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    _check(st)
+    return dq, dk, dv
+
+
+def attn_bwd_workspace_size(B: int, H: int, Nq: int) -> int:
+    return int(load_library().attn_bwd_workspace_size(B, H, Nq))
 
 
 def paged_decode_workspace_size(num_seqs: int, H: int, Hkv: int, d: int,

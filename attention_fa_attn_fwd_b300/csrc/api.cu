@@ -179,6 +179,46 @@ attn_status paged_prefill(const void* q, const void* k_cache, const void* v_cach
   return ATTN_OK;
 }
 
+size_t attn_bwd_workspace_size(int B, int H, int Nq) {
+  if (B < 1 || H < 1 || Nq < 1) return 0;
+  return attn::backward_workspace_bytes(B, H, Nq);
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq,
+                     int Nk, int d, float scale, int causal, void* workspace,
+                     size_t workspace_bytes, attn_stream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+    return fail(ATTN_EINVAL, "attn_bwd: null pointer argument");
+  if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < 1)
+    return fail(ATTN_EINVAL, "attn_bwd: sizes must be >= 1 (B=%d H=%d Hkv=%d Nq=%d Nk=%d)", B, H,
+                Hkv, Nq, Nk);
+  if (H % Hkv != 0) return fail(ATTN_EINVAL, "attn_bwd: H=%d is not a multiple of Hkv=%d", H, Hkv);
+  if (!(scale > 0.f) || !(scale < 3.0e38f))
+    return fail(ATTN_EINVAL, "attn_bwd: scale must be positive and finite");
+  if (causal != 0 && causal != 1) return fail(ATTN_EINVAL, "attn_bwd: causal must be 0 or 1");
+  if (d != 64 && d != 128) return fail(ATTN_EUNSUPPORTED, "attn_bwd: head dim %d (need 64 or 128)", d);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(workspace, 16))
+    return fail(ATTN_EINVAL, "attn_bwd: misaligned pointer");
+  if ((long long)B * H * ((Nq + 127) / 128) >= (1LL << 31) ||
+      (long long)B * Hkv * ((Nk + 127) / 128) >= (1LL << 31))
+    return fail(ATTN_EINVAL, "attn_bwd: problem too large");
+  const size_t need = attn::backward_workspace_bytes(B, H, Nq);
+  if (workspace_bytes < need)
+    return fail(ATTN_EINVAL, "attn_bwd: workspace %zu bytes < required %zu", workspace_bytes, need);
+  attn_status st = check_device();
+  if (st != ATTN_OK) return st;
+  const char* err = nullptr;
+  cudaError_t e = attn::backward_launch(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, Nq, Nk, d,
+                                        scale, causal, workspace,
+                                        reinterpret_cast<cudaStream_t>(stream), &err);
+  if (err) return fail(ATTN_ECUDA, "attn_bwd: %s", err);
+  if (e != cudaSuccess) return fail(ATTN_ECUDA, "attn_bwd launch: %s", cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
 size_t paged_decode_workspace_size(int num_seqs, int H, int Hkv, int d, int max_blocks_per_seq) {
   if (num_seqs < 1 || H < 1 || Hkv < 1 || H % Hkv || max_blocks_per_seq < 1 || (d != 64 && d != 128))
     return 0;
@@ -226,8 +266,10 @@ attn_status attn_device_status(attn_stream_t stream) {
   if (e != cudaSuccess) return fail(ATTN_ECUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
   const int a = attn::prefill_take_device_error();
   const int b = attn::decode_take_device_error();
-  if (a < 0 || b < 0) return fail(ATTN_ECUDA, "reading the device error word failed");
-  if (a || b) return fail(ATTN_EDEVICE, "device error: prefill 0x%x, decode 0x%x", a, b);
+  const int c = attn::backward_take_device_error();
+  if (a < 0 || b < 0 || c < 0) return fail(ATTN_ECUDA, "reading the device error word failed");
+  if (a || b || c)
+    return fail(ATTN_EDEVICE, "device error: prefill 0x%x, decode 0x%x, backward 0x%x", a, b, c);
   return ATTN_OK;
 }
 

@@ -39,6 +39,14 @@ cudaError_t decode_launch(const void* q, const void* k_cache, const void* v_cach
                           cudaStream_t stream, const char** err);
 int decode_take_device_error();
 
+// ---- backward (backward_sm103.cu)
+size_t backward_workspace_bytes(int B, int H, int Nq);
+cudaError_t backward_launch(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                            int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                            void* workspace, cudaStream_t stream, const char** err);
+int backward_take_device_error();
+
 // Sets the calling thread's attn_last_error() message (printf-style).
 void set_last_error(const char* fmt, ...);
 

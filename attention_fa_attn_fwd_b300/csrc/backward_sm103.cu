@@ -1,0 +1,767 @@
+// Attention backward pass for sm_103a (B300): dQ, dK, dV by recomputation.
+//
+// The forward pass keeps only O and the per-row log-sum-exp; the backward
+// pass recomputes P from Q, K and that statistic instead of reading a stored
+// N x N matrix (interview notes "他人面经整理", flashattention answer part 3,
+// recomputation for the backward pass; FAQ page "Wie unterscheidet sich die
+// Implementierung von FlashAttention-2 ...", comparison table, backward row).
+// With S = scale Q K^T (masked) and P = softmax(S):
+//   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  D_i = rowsum(dO_i o O_i),
+//   dQ = scale dS K,  dK = scale dS^T Q,
+// and a KV head's gradient sums over the query heads that read it (GQA).
+//
+// Three kernels, all on the caller's stream, no atomics (deterministic):
+//   bwd_delta_kernel   D = rowsum(dO o O) in fp32 (bandwidth-bound) into the
+//                      workspace.
+//   bwd_dq_kernel      Q-stationary: a CTA owns 128 query rows of one head and
+//                      streams the K/V tiles they attend: S = Q K^T and
+//                      dP = dO V^T into TMEM, dS (bf16) back into TMEM,
+//                      dQ += dS K accumulated in TMEM.
+//   bwd_dkdv_kernel    KV-stationary: a CTA owns 128 keys of one KV head and
+//                      streams, for every query head of its group, the Q/dO
+//                      tiles that attend them: S^T = K Q^T and dP^T = V dO^T,
+//                      P^T and dS^T (bf16) back into TMEM, dV += P^T dO and
+//                      dK += dS^T Q accumulated in TMEM.
+// Splitting dQ from dK/dV recomputes S and dP once more (7 instead of 5
+// matrix products) but keeps every accumulator in TMEM (dQ would need a
+// fifth 128-column TMEM block or fp32 atomics in the KV-stationary kernel).
+//
+// Warp roles in both tcgen05 kernels (12 warps): warp 0 TMA producer, warp 1
+// MMA issuer (one elected lane), warps 2-3 idle, warps 4-7 and 8-11 two
+// compute warpgroups that split the 128 score columns of every tile in
+// halves (thread r of a warpgroup owns TMEM lane / row r).  The compute
+// warpgroups write their bf16 results over the first 32 columns of their own
+// 64-column half, so the two never touch each other's columns.
+
+#include <cmath>
+#include <cstdio>
+
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+__device__ int g_backward_error;
+
+namespace {
+
+constexpr float kLog2e = 1.44269504088896340736f;
+
+template <int D>
+struct BCfg {
+  static constexpr int kSlabs = D / 64;
+  static constexpr int kSlabBytes = 128 * 128;             // 128 rows x 64 bf16
+  static constexpr int kTileBytes = kSlabs * kSlabBytes;   // one 128-row tile
+  static constexpr int kThreads = 384;
+  static constexpr int kRegsLow = 80;
+  static constexpr int kRegsHigh = 208;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+// ---------------------------------------------------------------- helpers
+
+// TMEM column of the bf16 A operand for the MMA over K-slice kk (16
+// elements): the two compute warpgroups packed their 64-element halves into
+// columns [0, 32) and [64, 96) of a 128-column block.
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+  return kk < 4 ? uint32_t(kk * 8) : uint32_t(64 + (kk - 4) * 8);
+}
+
+// 128-byte-swizzled row write of 32 fp32 values (scaled, rounded to bf16)
+// into a 128-row staging tile laid out in 64-column slabs.
+template <int D>
+__device__ __forceinline__ void stage_row32(uint8_t* tile, int row, int c0, const uint32_t* v,
+                                            float mul) {
+  uint32_t pw[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    pw[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+  uint8_t* rowp = tile + (c0 >> 6) * BCfg<D>::kSlabBytes + row * 128;
+  const int chunk0 = (c0 & 63) >> 3;
+#pragma unroll
+  for (int qd = 0; qd < 4; ++qd) {
+    const int ch = (chunk0 + qd) ^ (row & 7);
+    *reinterpret_cast<uint4*>(rowp + ch * 16) =
+        make_uint4(pw[4 * qd], pw[4 * qd + 1], pw[4 * qd + 2], pw[4 * qd + 3]);
+  }
+}
+
+struct BArgs {
+  const float* lse;  // [B, H, Nq] natural log, from the forward pass
+  float* delta;      // [B, H, Nq] workspace: rowsum(dO o O)
+  int B, H, Hkv, Nq, Nk;
+  float c_log2;  // scale * log2(e)
+  float scale;
+  int causal;
+};
+
+// -log2-domain LSE: P = 2^(s * c_log2 + neg_lse2).  A row with no key
+// (lse = -inf) gets -inf, i.e. P = 0.
+__device__ __forceinline__ float neg_lse2_of(float lse) {
+  return (lse == -INFINITY) ? -INFINITY : -lse * kLog2e;
+}
+
+// ================================================================ delta
+// D[row] = sum_c dO[row, c] * O[row, c]; D/8 threads per row, 16-byte loads.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restrict__ o,
+                                                        const uint16_t* __restrict__ dout,
+                                                        float* __restrict__ delta, long long rows) {
+  constexpr int TPR = D / 8;  // threads per row
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = t / TPR;
+  const int part = int(t % TPR);
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + part * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(dout + row * D + part * 8);
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc += __uint_as_float(av[e] << 16) * __uint_as_float(bv[e] << 16);
+      acc += __uint_as_float(av[e] & 0xffff0000u) * __uint_as_float(bv[e] & 0xffff0000u);
+    }
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && part == 0) delta[row] = acc;
+}
+
+// ================================================================ dQ
+template <int D>
+struct DqCfg : BCfg<D> {
+  using B_ = BCfg<D>;
+  static constexpr int kKStages = (D == 128) ? 2 : 4;
+  static constexpr int kVStages = (D == 128) ? 2 : 3;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = B_::kTileBytes;
+  static constexpr int kOffK = 2 * B_::kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * B_::kTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * B_::kTileBytes;
+  static constexpr int kBarQF = 0;
+  static constexpr int kBarKF = 1;
+  static constexpr int kBarKE = kBarKF + kKStages;
+  static constexpr int kBarVF = kBarKE + kKStages;
+  static constexpr int kBarVE = kBarVF + kVStages;
+  static constexpr int kBarSF = kBarVE + kVStages;  // S and dP in TMEM
+  static constexpr int kBarPF = kBarSF + 1;         // dS written (256 arrivals)
+  static constexpr int kBarOF = kBarPF + 1;         // dQ complete
+  static constexpr int kBarDrain = kBarOF + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+};
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_dq, const BArgs a) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  int* err = &g_backward_error;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Heavy (late, causal) query tiles first; heads of one KV group adjacent.
+  const int BH = a.B * a.H;
+  const int n_qt = (a.Nq + 127) / 128;
+  const int bh = blockIdx.x % BH;
+  const int q0 = (n_qt - 1 - int(blockIdx.x / BH)) * 128;
+  const int b = bh / a.H, h = bh % a.H;
+  const int zkv = b * a.Hkv + h / (a.H / a.Hkv);
+  const bool dead = timed_out_before(err);
+  int kv_end = a.Nk;
+  if (a.causal) kv_end = min(a.Nk, q0 + 128 + (a.Nk - a.Nq));
+  const int n = (kv_end > 0 && !dead) ? (kv_end + 127) / 128 : 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i) mbar_init(bar(i), i == C::kBarPF ? 256u : 1u);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_do);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_dq);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    setmaxnreg_dec<C::kRegsLow>();
+    if (warp == 0 && n > 0) {
+      // ------------------------------------------------------ producer
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      mbar_arrive_expect_tx_elect(bar(C::kBarQF), 2 * C::kTileBytes);
+      for (int s = 0; s < C::kSlabs; ++s) {
+        tma_load_3d_elect(sbase + C::kOffQ + s * C::kSlabBytes, &tm_q, bar(C::kBarQF), s * 64, q0, bh);
+        tma_load_3d_elect(sbase + C::kOffDO + s * C::kSlabBytes, &tm_do, bar(C::kBarQF), s * 64, q0,
+                          bh);
+      }
+      for (int j = 0; j < n; ++j) {
+        const int ks = j % C::kKStages, vs = j % C::kVStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarKE + ks), ((j / C::kKStages) & 1) ^ 1,
+                                               abort_flag, err, kErrTimeoutProducer));
+        if (!ok) break;
+        mbar_arrive_expect_tx_elect(bar(C::kBarKF + ks), C::kTileBytes);
+        for (int s = 0; s < C::kSlabs; ++s)
+          tma_load_3d_elect(sbase + C::kOffK + ks * C::kTileBytes + s * C::kSlabBytes, &tm_k,
+                            bar(C::kBarKF + ks), s * 64, j * 128, zkv);
+        k_issued = j + 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarVE + vs), ((j / C::kVStages) & 1) ^ 1,
+                                               abort_flag, err, kErrTimeoutProducer));
+        if (!ok) break;
+        mbar_arrive_expect_tx_elect(bar(C::kBarVF + vs), C::kTileBytes);
+        for (int s = 0; s < C::kSlabs; ++s)
+          tma_load_3d_elect(sbase + C::kOffV + vs * C::kTileBytes + s * C::kSlabBytes, &tm_v,
+                            bar(C::kBarVF + vs), s * 64, j * 128, zkv);
+        v_issued = j + 1;
+      }
+      if (!ok) {
+        const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
+        mbar_wait_drain(bar(C::kBarQF), 0, deadline);
+        for (int j = max(0, k_issued - C::kKStages); j < k_issued; ++j)
+          mbar_wait_drain(bar(C::kBarKF + j % C::kKStages), (j / C::kKStages) & 1, deadline);
+        for (int j = max(0, v_issued - C::kVStages); j < v_issued; ++j)
+          mbar_wait_drain(bar(C::kBarVF + j % C::kVStages), (j / C::kVStages) & 1, deadline);
+      }
+    } else if (warp == 1 && n > 0) {
+      // ------------------------------------------------------ MMA issuer
+      constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, 0);
+      constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, 1);
+      const uint64_t q_desc = smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
+      const uint64_t do_desc = smem_desc_sw128(sbase + C::kOffDO, 16, 1024);
+      const uint64_t k_desc = smem_desc_sw128(sbase + C::kOffK, 16, 1024);
+      const uint64_t v_desc = smem_desc_sw128(sbase + C::kOffV, 16, 1024);
+      const uint64_t kmn_desc = smem_desc_sw128(sbase + C::kOffK, C::kSlabBytes, 1024);
+      bool ok = __all_sync(0xffffffffu,
+                           mbar_wait(bar(C::kBarQF), 0, abort_flag, err, kErrTimeoutMma));
+      for (int j = 0; ok && j < n; ++j) {
+        const int ks = j % C::kKStages, vs = j % C::kVStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarKF + ks), (j / C::kKStages) & 1,
+                                               abort_flag, err, kErrTimeoutMma));
+        if (!ok) break;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarVF + vs), (j / C::kVStages) & 1,
+                                               abort_flag, err, kErrTimeoutMma));
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t ko = uint64_t((ks * C::kTileBytes) >> 4);
+        const uint64_t vo = uint64_t((vs * C::kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // S = Q K_j^T
+          const uint64_t off = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + C::kColS, q_desc + off, k_desc + ko + off, kIdescSS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V_j^T
+          const uint64_t off = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + C::kColDP, do_desc + off, v_desc + vo + off, kIdescSS,
+                      kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBarSF));
+        mma_commit(bar(C::kBarVE + vs));
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(C::kBarPF), j & 1, abort_flag, err, kErrTimeoutMma));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j (16 keys per MMA)
+          mma_bf16_ts(tmem + C::kColDQ, tmem + C::kColS + packed_col(kk),
+                      kmn_desc + ko + uint64_t((kk * 2048) >> 4), kIdescDQ,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(C::kBarKE + ks));
+      }
+      if (ok) {
+        mma_commit(bar(C::kBarOF));
+      } else {
+        mma_commit(bar(C::kBarDrain));
+        mbar_wait_drain(bar(C::kBarDrain), 0, globaltimer_ns() + kWaitTimeoutNs);
+      }
+    }
+  } else {
+    setmaxnreg_inc<C::kRegsHigh>();
+    // -------------------------------------------------------- compute
+    const int wg = (warp >> 2) - 1;   // which 64-column half
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
+    const int q_row = q0 + row;
+    const int row_last = a.causal ? min(a.Nk - 1, q_row + (a.Nk - a.Nq)) : (a.Nk - 1);
+    float neg_lse2 = -INFINITY, drow = 0.f;
+    if (q_row < a.Nq) {
+      neg_lse2 = neg_lse2_of(a.lse[size_t(bh) * a.Nq + q_row]);
+      drow = a.delta[size_t(bh) * a.Nq + q_row];
+    }
+    const float c = a.c_log2;
+    bool ok = !dead;
+    for (int j = 0; ok && j < n; ++j) {
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::kBarSF), j & 1, abort_flag, err, kErrTimeoutSoftmax));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[64], p[64];
+      tmem_ld32(lane_base + C::kColS + wg * 64, s);
+      tmem_ld32(lane_base + C::kColS + wg * 64 + 32, s + 32);
+      tmem_ld32(lane_base + C::kColDP + wg * 64, p);
+      tmem_ld32(lane_base + C::kColDP + wg * 64 + 32, p + 32);
+      tmem_ld_wait();
+      reg_fence<64>(s);
+      reg_fence<64>(p);
+      const int lim = row_last - j * 128 - wg * 64;  // columns > lim are masked
+      uint32_t pk[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        float x0 = ex2_approx(fmaf(__uint_as_float(s[2 * e]), c, neg_lse2));
+        float x1 = ex2_approx(fmaf(__uint_as_float(s[2 * e + 1]), c, neg_lse2));
+        if (2 * e > lim) x0 = 0.f;
+        if (2 * e + 1 > lim) x1 = 0.f;
+        const float d0 = x0 * (__uint_as_float(p[2 * e]) - drow);
+        const float d1 = x1 * (__uint_as_float(p[2 * e + 1]) - drow);
+        pk[e] = pack_bf16x2(d0, d1);
+      }
+      tmem_st32(lane_base + C::kColS + wg * 64, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarPF));
+    }
+    // -------------------------------------------------------- epilogue
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::kBarOF), 0, abort_flag, err, kErrTimeoutEpilogue));
+      tc_fence_after();
+    }
+    uint8_t* stage = smem + C::kOffQ;  // Q is no longer read once dQ is complete
+    if (ok) {
+#pragma unroll
+      for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
+        uint32_t v[32];
+        if (n > 0) {
+          tmem_ld32(lane_base + C::kColDQ + c0, v);
+          tmem_ld_wait();
+          reg_fence<32>(v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        stage_row32<D>(stage, row, c0, v, a.scale);
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1, 256);
+    if (!*abort_flag && ok && warp == 4 && lane == 0) {
+      for (int s = 0; s < C::kSlabs; ++s)
+        tma_store_3d(&tm_dq, sbase + C::kOffQ + s * C::kSlabBytes, s * 64, q0, bh);
+      bulk_commit_group();
+      bulk_wait_group_read0();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ================================================================ dK, dV
+template <int D>
+struct DkvCfg : BCfg<D> {
+  using B_ = BCfg<D>;
+  static constexpr int kQStages = (D == 128) ? 2 : 3;  // (Q, dO, -lse2, D) per stage
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = B_::kTileBytes;
+  static constexpr int kOffQ = 2 * B_::kTileBytes;                       // Q stages
+  static constexpr int kOffDO = kOffQ + kQStages * B_::kTileBytes;       // dO stages
+  static constexpr int kOffStat = kOffDO + kQStages * B_::kTileBytes;    // [stage][2][128] fp32
+  static constexpr int kOffBar = kOffStat + kQStages * 2 * 128 * 4;
+  static constexpr int kBarKVF = 0;
+  static constexpr int kBarQF = 1;
+  static constexpr int kBarQE = kBarQF + kQStages;
+  static constexpr int kBarSF = kBarQE + kQStages;  // S^T and dP^T in TMEM
+  static constexpr int kBarPF = kBarSF + 1;         // P^T, dS^T written (256 arrivals)
+  static constexpr int kBarOF = kBarPF + 1;         // dK, dV complete
+  static constexpr int kBarDrain = kBarOF + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+};
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv, const BArgs a) {
+  using C = DkvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  float* stat = reinterpret_cast<float*>(smem + C::kOffStat);
+  int* err = &g_backward_error;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // CTA = (KV tile, b, KV head); causal: early key tiles (most query tiles) first.
+  const int BK = a.B * a.Hkv;
+  const int zkv = blockIdx.x % BK;
+  const int k0 = int(blockIdx.x / BK) * 128;
+  const int b = zkv / a.Hkv, g = zkv % a.Hkv;
+  const int G = a.H / a.Hkv;
+  const int off = a.Nk - a.Nq;  // query row i sees keys j <= i + off (causal)
+  const int n_qt = (a.Nq + 127) / 128;
+  int qt0 = 0;
+  if (a.causal) {
+    const int first_row = k0 - off;  // first query row that sees key k0
+    qt0 = first_row <= 0 ? 0 : first_row / 128;
+  }
+  const bool dead = timed_out_before(err);
+  const int per_head = max(0, n_qt - qt0);
+  const int n_it = dead ? 0 : G * per_head;  // (query head, query tile) pairs
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i) {
+      uint32_t cnt = 1;
+      if (i == C::kBarPF) cnt = 256;
+      if (i >= C::kBarQF && i < C::kBarQF + C::kQStages) cnt = 32;
+      mbar_init(bar(i), cnt);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_do);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_dk);
+    prefetch_tmap(&tm_dv);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    setmaxnreg_dec<C::kRegsLow>();
+    if (warp == 0 && n_it > 0) {
+      // ------------------------------------------------------ producer
+      mbar_arrive_expect_tx_elect(bar(C::kBarKVF), 2 * C::kTileBytes);
+      for (int s = 0; s < C::kSlabs; ++s) {
+        tma_load_3d_elect(sbase + C::kOffK + s * C::kSlabBytes, &tm_k, bar(C::kBarKVF), s * 64, k0,
+                          zkv);
+        tma_load_3d_elect(sbase + C::kOffV + s * C::kSlabBytes, &tm_v, bar(C::kBarKVF), s * 64, k0,
+                          zkv);
+      }
+      bool ok = true;
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it % C::kQStages;
+        const int hq = b * a.H + g * G + it / per_head;  // query (b, h) row of the tensor maps
+        const int r0 = (qt0 + it % per_head) * 128;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarQE + st), ((it / C::kQStages) & 1) ^ 1,
+                                               abort_flag, err, kErrTimeoutProducer));
+        if (!ok) break;
+        // Row statistics of the 128 queries: -lse*log2(e) (-inf past Nq) and D.
+        float* sp = stat + st * 256;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int cidx = lane * 4 + e;
+          const int r = r0 + cidx;
+          float nl = -INFINITY, dd = 0.f;
+          if (r < a.Nq) {
+            nl = neg_lse2_of(a.lse[size_t(hq) * a.Nq + r]);
+            dd = a.delta[size_t(hq) * a.Nq + r];
+          }
+          sp[cidx] = nl;
+          sp[128 + cidx] = dd;
+        }
+        if (lane == 0)
+          mbar_arrive_expect_tx(bar(C::kBarQF + st), 2 * C::kTileBytes);
+        else
+          mbar_arrive(bar(C::kBarQF + st));
+        __syncwarp();
+        for (int s = 0; s < C::kSlabs; ++s) {
+          tma_load_3d_elect(sbase + C::kOffQ + st * C::kTileBytes + s * C::kSlabBytes, &tm_q,
+                            bar(C::kBarQF + st), s * 64, r0, hq);
+          tma_load_3d_elect(sbase + C::kOffDO + st * C::kTileBytes + s * C::kSlabBytes, &tm_do,
+                            bar(C::kBarQF + st), s * 64, r0, hq);
+        }
+        issued = it + 1;
+      }
+      if (!ok) {
+        const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
+        mbar_wait_drain(bar(C::kBarKVF), 0, deadline);
+        for (int it = max(0, issued - C::kQStages); it < issued; ++it)
+          mbar_wait_drain(bar(C::kBarQF + it % C::kQStages), (it / C::kQStages) & 1, deadline);
+      }
+    } else if (warp == 1 && n_it > 0) {
+      // ------------------------------------------------------ MMA issuer
+      constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, 0);
+      constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 1);
+      const uint64_t k_desc = smem_desc_sw128(sbase + C::kOffK, 16, 1024);
+      const uint64_t v_desc = smem_desc_sw128(sbase + C::kOffV, 16, 1024);
+      const uint64_t q_desc = smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
+      const uint64_t do_desc = smem_desc_sw128(sbase + C::kOffDO, 16, 1024);
+      const uint64_t qmn_desc = smem_desc_sw128(sbase + C::kOffQ, C::kSlabBytes, 1024);
+      const uint64_t domn_desc = smem_desc_sw128(sbase + C::kOffDO, C::kSlabBytes, 1024);
+      bool ok = __all_sync(0xffffffffu,
+                           mbar_wait(bar(C::kBarKVF), 0, abort_flag, err, kErrTimeoutMma));
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int st = it % C::kQStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarQF + st), (it / C::kQStages) & 1,
+                                               abort_flag, err, kErrTimeoutMma));
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t so = uint64_t((st * C::kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K Q^T, dP^T = V dO^T
+          const uint64_t o16 = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + C::kColS, k_desc + o16, q_desc + so + o16, kIdescSS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t o16 = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + C::kColDP, v_desc + o16, do_desc + so + o16, kIdescSS,
+                      kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBarSF));
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(C::kBarPF), it & 1, abort_flag, err, kErrTimeoutMma));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // dV += P^T dO, dK += dS^T Q (16 queries per MMA)
+          const uint64_t o16 = so + uint64_t((kk * 2048) >> 4);
+          mma_bf16_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(kk), domn_desc + o16,
+                      kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col(kk), qmn_desc + o16,
+                      kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBarQE + st));
+      }
+      if (ok) {
+        mma_commit(bar(C::kBarOF));
+      } else {
+        mma_commit(bar(C::kBarDrain));
+        mbar_wait_drain(bar(C::kBarDrain), 0, globaltimer_ns() + kWaitTimeoutNs);
+      }
+    }
+  } else {
+    setmaxnreg_inc<C::kRegsHigh>();
+    // -------------------------------------------------------- compute
+    const int wg = (warp >> 2) - 1;  // which 64-query half of the tile
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // key within the tile
+    const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
+    const int kj = k0 + row;
+    const float c = a.c_log2;
+    bool ok = !dead;
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int st = it % C::kQStages;
+      const int r0 = (qt0 + it % per_head) * 128;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarQF + st), (it / C::kQStages) & 1,
+                                             abort_flag, err, kErrTimeoutSoftmax));
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::kBarSF), it & 1, abort_flag, err, kErrTimeoutSoftmax));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[64], p[64];
+      tmem_ld32(lane_base + C::kColS + wg * 64, s);
+      tmem_ld32(lane_base + C::kColS + wg * 64 + 32, s + 32);
+      tmem_ld32(lane_base + C::kColDP + wg * 64, p);
+      tmem_ld32(lane_base + C::kColDP + wg * 64 + 32, p + 32);
+      tmem_ld_wait();
+      reg_fence<64>(s);
+      reg_fence<64>(p);
+      const float* nl = stat + st * 256 + wg * 64;
+      const float* dd = nl + 128;
+      // Column q (query r0 + wg*64 + q) is masked if this key is past Nk or,
+      // causally, if kj > query + off, i.e. q < kj - off - r0 - wg*64.
+      const int lo = a.causal ? (kj - off - r0 - wg * 64) : -1;
+      const bool key_ok = kj < a.Nk;
+      uint32_t pp[32], pd[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        float x0 = ex2_approx(fmaf(__uint_as_float(s[2 * e]), c, nl[2 * e]));
+        float x1 = ex2_approx(fmaf(__uint_as_float(s[2 * e + 1]), c, nl[2 * e + 1]));
+        if (!key_ok || 2 * e < lo) x0 = 0.f;
+        if (!key_ok || 2 * e + 1 < lo) x1 = 0.f;
+        pp[e] = pack_bf16x2(x0, x1);
+        pd[e] = pack_bf16x2(x0 * (__uint_as_float(p[2 * e]) - dd[2 * e]),
+                            x1 * (__uint_as_float(p[2 * e + 1]) - dd[2 * e + 1]));
+      }
+      tmem_st32(lane_base + C::kColS + wg * 64, pp);
+      tmem_st32(lane_base + C::kColDP + wg * 64, pd);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarPF));
+    }
+    // -------------------------------------------------------- epilogue
+    if (ok && n_it > 0) {
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::kBarOF), 0, abort_flag, err, kErrTimeoutEpilogue));
+      tc_fence_after();
+    }
+    // wg 0 writes dV through Q stage 0, wg 1 writes scale * dK through dO stage 0.
+    uint8_t* stage = smem + (wg == 0 ? C::kOffQ : C::kOffDO);
+    const uint32_t col = wg == 0 ? C::kColDV : C::kColDK;
+    const float mul = wg == 0 ? 1.f : a.scale;
+    if (ok) {
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t v[32];
+        if (n_it > 0) {
+          tmem_ld32(lane_base + col + c0, v);
+          tmem_ld_wait();
+          reg_fence<32>(v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        stage_row32<D>(stage, row, c0, v, mul);
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1 + wg, 128);
+    if (!*abort_flag && ok && quarter == 0 && lane == 0) {
+      const CUtensorMap* tm = wg == 0 ? &tm_dv : &tm_dk;
+      const uint32_t src = sbase + (wg == 0 ? C::kOffQ : C::kOffDO);
+      for (int s = 0; s < C::kSlabs; ++s)
+        tma_store_3d(tm, src + s * C::kSlabBytes, s * 64, k0, zkv);
+      bulk_commit_group();
+      bulk_wait_group_read0();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ================================================================ launch
+
+template <typename K>
+cudaError_t set_smem_once(K kernel, int bytes, int* configured) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (*configured != dev) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    *configured = dev;
+  }
+  return cudaSuccess;
+}
+
+template <int D>
+cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int H, int Hkv, int Nq, int Nk, float scale, int causal, float* delta,
+                       cudaStream_t stream, const char** err) {
+  const uint32_t box[3] = {64, 128, 1};
+  const uint64_t dq_[3] = {uint64_t(D), uint64_t(Nq), uint64_t(B) * H};
+  const uint64_t sq[2] = {uint64_t(D) * 2, uint64_t(Nq) * D * 2};
+  const uint64_t dk_[3] = {uint64_t(D), uint64_t(Nk), uint64_t(B) * Hkv};
+  const uint64_t sk[2] = {uint64_t(D) * 2, uint64_t(Nk) * D * 2};
+  CUtensorMap tq, tdo, tk, tv, tdq, tdk, tdv;
+  if (!encode_tmap_bf16(&tq, q, 3, dq_, sq, box, true, err) ||
+      !encode_tmap_bf16(&tdo, dout, 3, dq_, sq, box, true, err) ||
+      !encode_tmap_bf16(&tdq, dq, 3, dq_, sq, box, true, err) ||
+      !encode_tmap_bf16(&tk, k, 3, dk_, sk, box, true, err) ||
+      !encode_tmap_bf16(&tv, v, 3, dk_, sk, box, true, err) ||
+      !encode_tmap_bf16(&tdk, dk, 3, dk_, sk, box, true, err) ||
+      !encode_tmap_bf16(&tdv, dv, 3, dk_, sk, box, true, err))
+    return cudaErrorInvalidValue;
+  static thread_local int conf_dq = -1, conf_dkdv = -1;
+  cudaError_t e = set_smem_once(bwd_dq_kernel<D>, DqCfg<D>::kSmemBytes, &conf_dq);
+  if (e != cudaSuccess) return e;
+  e = set_smem_once(bwd_dkdv_kernel<D>, DkvCfg<D>::kSmemBytes, &conf_dkdv);
+  if (e != cudaSuccess) return e;
+
+  BArgs a;
+  a.lse = lse;
+  a.delta = delta;
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.c_log2 = scale * kLog2e;
+  a.scale = scale;
+  a.causal = causal;
+
+  const long long rows = (long long)B * H * Nq;
+  const long long threads = rows * (D / 8);
+  bwd_delta_kernel<D><<<unsigned((threads + 255) / 256), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta, rows);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const unsigned grid_dq = unsigned(B) * H * unsigned((Nq + 127) / 128);
+  bwd_dq_kernel<D><<<grid_dq, 384, DqCfg<D>::kSmemBytes, stream>>>(tq, tdo, tk, tv, tdq, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const unsigned grid_kv = unsigned(B) * Hkv * unsigned((Nk + 127) / 128);
+  bwd_dkdv_kernel<D><<<grid_kv, 384, DkvCfg<D>::kSmemBytes, stream>>>(tq, tdo, tk, tv, tdk, tdv,
+                                                                       a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t backward_workspace_bytes(int B, int H, int Nq) {
+  const size_t n = size_t(B) * H * Nq * sizeof(float);
+  return (n + 255) / 256 * 256;
+}
+
+cudaError_t backward_launch(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                            int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                            void* workspace, cudaStream_t stream, const char** err) {
+  float* delta = static_cast<float*>(workspace);
+  if (d == 128)
+    return launch_bwd<128>(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, Nq, Nk, scale, causal,
+                           delta, stream, err);
+  return launch_bwd<64>(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, Nq, Nk, scale, causal, delta,
+                        stream, err);
+}
+
+int backward_take_device_error() {
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_backward_error, sizeof(int)) != cudaSuccess) return -1;
+  if (v != 0) cudaMemcpyToSymbol(g_backward_error, &zero, sizeof(int));
+  return v;
+}
+
+}  // namespace attn

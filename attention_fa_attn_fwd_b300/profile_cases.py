@@ -9,6 +9,7 @@
 N16384 d128; 335 MB on the device, larger than L2).  ``decode``: paged_decode
 on the 64-sequence workload (2.3 GB pool).  ``step``: both, as one bench step.
 ``paged_prefill``: chunked prefill of 8 x 2048 tokens over a paged cache.
+``backward``: attn_bwd on the prefill workload (after one untimed attn_fwd).
 A 256 MiB L2 flush (a memset, not one of this library's kernels) precedes
 every kernel, as in bench.py.  Prints the CUDA-event time of each launch.
 """
@@ -25,7 +26,7 @@ from . import binding, workloads
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=["prefill", "decode", "step", "paged_prefill"], default="step")
+    ap.add_argument("--case", choices=["prefill", "decode", "step", "paged_prefill", "backward"], default="step")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--prefill", default="gqa_b1h32kv8_n16384_d128_causal")
     ap.add_argument("--decode-seqs", type=int, default=64,
@@ -63,6 +64,16 @@ def main(argv=None):
         pl = torch.empty(pq.shape[:3], dtype=torch.float32, device=dev)
         runs.append(("paged_prefill", lambda: binding.paged_prefill(pq, pkc, pvc, pbt, psl,
                                                                     o=po, lse=pl)))
+    if args.case == "backward":
+        cfg = dict(workloads.PREFILL_WORKLOADS.get(args.prefill) or workloads.sweep_workloads()[args.prefill])
+        q, k, v = (t.to(dev) for t in workloads.prefill_inputs(**cfg))
+        do = workloads.grad_output(q.shape).to(dev)
+        o, lse = binding.attn_fwd(q, k, v, causal=cfg["causal"])
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bws = torch.empty(binding.attn_bwd_workspace_size(*q.shape[:3]), dtype=torch.uint8,
+                          device=dev)
+        runs.append(("attn_bwd", lambda: binding.attn_bwd(q, k, v, o, do, lse, causal=cfg["causal"],
+                                                          dq=dq, dk=dk, dv=dv, workspace=bws)))
     for it in range(args.iters):
         for name, fn in runs:
             flush.zero_()

@@ -86,6 +86,13 @@ def prefill_inputs(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int,
     return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
 
 
+def grad_output(shape, seed: int = 0) -> torch.Tensor:
+    """dL/dO for the backward pass: bfloat16 N(0, 1) of ``shape`` from its own
+    generator (seed + 7919), so Q, K, V of the same seed are unchanged."""
+    g = torch.Generator("cpu").manual_seed(seed + 7919)
+    return torch.randn(*shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
 @dataclasses.dataclass
 class PagedBatch:
     q: torch.Tensor               # [S, H, d] bf16 (decode) or [S, H, Nq, d] (chunked prefill)

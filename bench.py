@@ -382,6 +382,34 @@ def run_ours(args, ws, rank, local):
     pp_tflops = pp_flops / (pp_ms * 1e-3) / 1e12
     del pq, pkc, pvc, pbt, psl, po, plse
 
+    # ---- backward pass of the prefill workload (reported beside the step)
+    do_ = workloads.grad_output(q_h.shape, seed=rank).to(dev)
+    dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bws = torch.empty(binding.attn_bwd_workspace_size(cfg["B"], cfg["H"], cfg["Nq"]),
+                      dtype=torch.uint8, device=dev)
+    prefill()
+
+    def backward():
+        binding.attn_bwd(q, k, v, o, do_, lse, causal=True, dq=dq_, dk=dk_, dv=dv_,
+                         workspace=bws, stream=stream)
+
+    for _ in range(3):
+        flush.zero_()
+        backward()
+    Kb = max(3, min(K, 50))
+    b_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kb)]
+    for i in range(Kb):
+        flush.zero_()
+        b_evs[i][0].record(stream)
+        backward()
+        b_evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert binding.device_status(stream) == 0
+    bw_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in b_evs), ws)
+    bw_flops = 2.5 * prefill_flops(cfg) * ws  # 5 matrix products vs the forward's 2
+    bw_tflops = bw_flops / (bw_ms * 1e-3) / 1e12
+    del do_, dq_, dk_, dv_, bws
+
     # ---- end to end through the public API with pinned host buffers
     qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
     op = torch.empty(q_h.shape, dtype=torch.bfloat16).pin_memory()
@@ -456,6 +484,10 @@ def run_ours(args, ws, rank, local):
                           "tflops": pp_tflops, "frac_burst": pp_tflops / ws / peak_tf,
                           "flops": pp_flops / ws, "kernel": "prefill_fwd_kernel<128, paged>",
                           "kv_lens": [int(x) for x in pp.seq_lens]},
+        "backward": {"workload": PREFILL, "ms": bw_ms, "tflops": bw_tflops,
+                     "frac_burst": bw_tflops / ws / peak_tf,
+                     "flops": bw_flops / ws, "flops_note": "algorithmic: 2.5 x forward (5 products)",
+                     "kernels": "bwd_delta_kernel + bwd_dq_kernel<128> + bwd_dkdv_kernel<128>"},
         "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "prefill_ms": ep, "decode_ms": ed,
                 "decode_gbs": ws * (uniq_bytes + small_bytes) / (ed * 1e-3) / 1e9},

@@ -81,6 +81,45 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                      attn_stream_t stream);
 
 /*
+ * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs (the
+ * per-row fp32 D = rowsum(dO o O), B*H*Nq floats rounded up to 256 bytes).
+ * Returns 0 for invalid sizes.  Pure host function.
+ */
+ATTN_API size_t attn_bwd_workspace_size(int B, int H, int Nq);
+
+/*
+ * attn_bwd -- gradients of attn_fwd: given dO = dL/dO, returns dQ, dK, dV,
+ * recomputing P from Q, K and the forward pass's LSE instead of storing it.
+ *
+ * Defined by: interview notes "他人面经整理", flashattention answer, part 3
+ * (the backward pass recomputes the attention matrix from Q, K, V and the
+ * softmax statistics) and FAQ page "Wie unterscheidet sich die
+ * Implementierung von FlashAttention-2 ...", comparison table (recomputation
+ * in the backward pass).  With S = scale Q K^T (masked as in attn_fwd) and
+ * P = softmax(S): dV = P^T dO, dP = dO V^T, D_i = rowsum(dO_i o O_i),
+ * dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q; a KV head's dK, dV
+ * sum over the H/Hkv query heads that read it.
+ *
+ *   q, o, dout, dq   [B, H,   Nq, d]  bf16 (dq output)
+ *   k, v, dk, dv     [B, Hkv, Nk, d]  bf16 (dk, dv outputs)
+ *   lse              [B, H,   Nq]     fp32, as written by attn_fwd (natural
+ *                    log; -inf for rows with no key)
+ *   o                attn_fwd's output for the same q, k, v, scale, causal
+ *   workspace        >= attn_bwd_workspace_size(B, H, Nq) bytes, 16-byte
+ *                    aligned, caller-owned; clobbered.
+ * Rows with no unmasked key get dq = 0 and contribute nothing to dk, dv.
+ * Deterministic: no atomics; identical calls give identical bits.
+ *
+ * Requirements: as attn_fwd (d in {64, 128}, H % Hkv == 0, pointers 16-byte
+ * aligned, lse 4-byte aligned); dq, dk, dv must not alias the inputs.
+ */
+ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                              int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
+                              int causal, void* workspace, size_t workspace_bytes,
+                              attn_stream_t stream);
+
+/*
  * paged_decode_workspace_size -- bytes of device workspace paged_decode needs
  * for these sizes (it holds the per-split partial results merged by LSE).
  * Returns 0 for invalid sizes.  Pure host function.

@@ -28,7 +28,8 @@ def lib():
 
 def test_header_declares_expected_api():
     assert declared_functions() == sorted(["attn_fwd", "paged_decode", "paged_decode_workspace_size",
-                                           "paged_decode_noalloc", "paged_prefill", "attn_last_error",
+                                           "paged_decode_noalloc", "paged_prefill", "attn_bwd",
+                                           "attn_bwd_workspace_size", "attn_last_error",
                                            "attn_device_status"])
 
 
@@ -140,3 +141,36 @@ def _pp(lib, **kw):
 def test_paged_prefill_rejects_bad_arguments(lib, kw, status):
     assert _pp(lib, **kw) == status
     assert lib.attn_last_error()
+
+
+def _bwd(lib, **kw):
+    a = dict(q=_fake(1), k=_fake(2), v=_fake(3), o=_fake(4), do=_fake(5), lse=_fake(6),
+             dq=_fake(7), dk=_fake(8), dv=_fake(9), B=1, H=4, Hkv=2, Nq=256, Nk=256, d=128,
+             scale=0.088, causal=1, ws=_fake(10), wsb=1 << 20, stream=None)
+    a.update(kw)
+    return lib.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"],
+                        a["dv"], a["B"], a["H"], a["Hkv"], a["Nq"], a["Nk"], a["d"], a["scale"],
+                        a["causal"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(do=None), binding.ATTN_EINVAL),
+    (dict(lse=None), binding.ATTN_EINVAL),
+    (dict(ws=None), binding.ATTN_EINVAL),
+    (dict(wsb=16), binding.ATTN_EINVAL),
+    (dict(Nk=0), binding.ATTN_EINVAL),
+    (dict(H=3), binding.ATTN_EINVAL),
+    (dict(d=32), binding.ATTN_EUNSUPPORTED),
+    (dict(causal=-1), binding.ATTN_EINVAL),
+    (dict(scale=0.0), binding.ATTN_EINVAL),
+    (dict(dk=ctypes.c_void_p(0x10004)), binding.ATTN_EINVAL),
+])
+def test_attn_bwd_rejects_bad_arguments(lib, kw, status):
+    assert _bwd(lib, **kw) == status
+    assert lib.attn_last_error()
+
+
+def test_bwd_workspace_size(lib):
+    assert lib.attn_bwd_workspace_size(2, 16, 2048) == 2 * 16 * 2048 * 4
+    assert lib.attn_bwd_workspace_size(1, 1, 1) == 256
+    assert lib.attn_bwd_workspace_size(0, 1, 1) == 0

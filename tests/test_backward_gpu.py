@@ -1,0 +1,90 @@
+"""GPU parity of attn_bwd (C ABI) against the fp64 backward oracle.
+
+The GPU path runs attn_fwd, then attn_bwd on its O and LSE; the oracle
+differentiates the definition in float64 from the same bf16 Q, K, V, dO.
+Tolerances: ``tests/parity.py`` (GRAD_REL_RMS, GRAD_MAX_REL).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_fa_attn_fwd_b300 import binding, workloads
+from tests.parity import compare_grad, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(q, k, v, do, causal, scale=None):
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = binding.attn_fwd(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = binding.attn_bwd(qd, kd, vd, o, dod, lse, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return dq.cpu(), dk.cpu(), dv.cpu()
+
+
+def check_bwd(B, H, Hkv, Nq, Nk, d, causal, seed=0, gain=1.0, scale=None, what=""):
+    q, k, v = workloads.prefill_inputs(B, H, Hkv, Nq, Nk, d, seed=seed, qk_gain=gain)
+    do = workloads.grad_output(q.shape, seed=seed)
+    sc = (1.0 / math.sqrt(d)) if scale is None else scale
+    dq, dk, dv = _run(q, k, v, do, causal, scale)
+    rq, rk, rv, _ = oracle.attention_bwd_ref(f64(q), f64(k), f64(v), f64(do), sc, causal)
+    return (compare_grad(f64(dq), rq, f"dq {what}"), compare_grad(f64(dk), rk, f"dk {what}"),
+            compare_grad(f64(dv), rv, f"dv {what}"))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny(causal):
+    check_bwd(1, 2, 2, 128, 128, 64, causal, what="tiny")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 17, 200, 383])
+def test_ragged_lengths(d, causal, N):
+    check_bwd(1, 2, 1, N, N, d, causal, seed=N + d, what=f"N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("Nq,Nk", [(100, 300), (300, 100), (1, 257), (256, 640)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_unequal_lengths(Nq, Nk, causal):
+    check_bwd(2, 4, 2, Nq, Nk, 128, causal, seed=Nq + 3 * Nk, what=f"Nq={Nq} Nk={Nk}")
+
+
+@pytest.mark.parametrize("H,Hkv", [(8, 1), (8, 2), (6, 3)])
+def test_gqa(H, Hkv):
+    check_bwd(1, H, Hkv, 384, 384, 128, True, seed=H + Hkv, what=f"H={H} Hkv={Hkv}")
+
+
+def test_peaky_and_nondefault_scale():
+    check_bwd(1, 2, 2, 512, 512, 128, True, seed=21, gain=2.0, what="gain 2")
+    check_bwd(1, 2, 2, 256, 256, 64, False, seed=22, scale=0.05, what="scale 0.05")
+
+
+def test_mid_size_causal_gqa():
+    check_bwd(1, 8, 2, 1024, 1024, 128, True, seed=23, what="B1 H8 Hkv2 N1024")
+
+
+def test_fully_masked_rows_give_zero_dq():
+    q, k, v = workloads.prefill_inputs(1, 2, 2, 300, 100, 64, seed=9)
+    do = workloads.grad_output(q.shape, seed=9)
+    dq, dk, dv = _run(q, k, v, do, True)
+    assert torch.all(dq[:, :, :200].float() == 0)
+    rq, rk, rv, _ = oracle.attention_bwd_ref(f64(q), f64(k), f64(v), f64(do), 1 / 8.0, True)
+    compare_grad(f64(dq), rq, "dq")
+    compare_grad(f64(dk), rk, "dk")
+    compare_grad(f64(dv), rv, "dv")
+
+
+def test_deterministic_and_status_clean():
+    q, k, v = (t.cuda() for t in workloads.prefill_inputs(2, 4, 2, 700, 700, 128, seed=13))
+    do = workloads.grad_output(q.shape, seed=13).cuda()
+    o, lse = binding.attn_fwd(q, k, v, causal=True)
+    a = binding.attn_bwd(q, k, v, o, do, lse, causal=True)
+    b = binding.attn_bwd(q, k, v, o, do, lse, causal=True)
+    torch.cuda.synchronize()
+    assert all(torch.equal(x, y) for x, y in zip(a, b))
+    assert binding.device_status() == binding.ATTN_OK
