@@ -21,6 +21,8 @@ Modules
                apply the definition.
 ``backward``   gradients of the definition (dQ, dK, dV) by the chain rule,
                with P materialised.
+``kv_cache``   appending tokens to a paged cache: the logical definition and
+               a sequential copy-on-write block manager.
 ``bf16``       exact decoding of bfloat16 bit patterns to float64.
 
 Every function states the passage of the source pages it follows.  Every
@@ -38,6 +40,7 @@ from .attention import (
     attention_online,
 )
 from .backward import attention_bwd_ref
+from .kv_cache import BlockManagerRef, append_logical
 from .paged import gather_logical_kv, paged_decode_ref, paged_decode_ref_from_pool, paged_prefill_ref
 
 __all__ = [
@@ -52,4 +55,6 @@ __all__ = [
     "paged_decode_ref_from_pool",
     "paged_prefill_ref",
     "attention_bwd_ref",
+    "append_logical",
+    "BlockManagerRef",
 ]
