@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     AttnError,
     attn_bwd,
     attn_fwd,
+    kv_append,
     paged_decode,
     paged_prefill,
     paged_decode_workspace_size,

@@ -45,6 +45,9 @@ SIGNATURES = {
     "attn_bwd_workspace_size": (_sz, [_i, _i, _i]),
     "attn_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i,
                       _vp, _sz, _vp]),
+    "kv_append_workspace_size": (_sz, [_i, _i]),
+    "kv_append": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                       _vp, _sz, _vp]),
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_device_status": (_i, [_vp]),
 }
@@ -315,6 +318,47 @@ def paged_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                            lse.data_ptr() if lse is not None else None, _stream_handle(stream))
     _check(st)
     return o, lse
+
+
+def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+              v_cache: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+              ref_counts: torch.Tensor, free_ids: torch.Tensor, free_top: torch.Tensor,
+              workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Append T tokens per sequence to a paged cache via ``kv_append`` (in place).
+
+    k_new/v_new [S,T,Hkv,d] bf16; caches [num_blocks,Hkv,16,d] bf16;
+    block_table [S,max_blocks], seq_lens [S], ref_counts [num_blocks],
+    free_ids [n], free_top [1] int32 -- all updated on the device.
+    """
+    lib = load_library()
+    _need(k_new, "k_new", torch.bfloat16, 4)
+    _need(v_new, "v_new", torch.bfloat16, 4)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(ref_counts, "ref_counts", torch.int32, 1)
+    _need(free_ids, "free_ids", torch.int32, 1)
+    _need(free_top, "free_top", torch.int32, 1)
+    S, T, Hkv, d = k_new.shape
+    num_blocks, hk, block_size, dk = k_cache.shape
+    if v_new.shape != k_new.shape or v_cache.shape != k_cache.shape or hk != Hkv or dk != d:
+        raise ValueError("kv_append: shape mismatch")
+    if block_table.shape[0] != S or seq_lens.shape[0] != S or ref_counts.shape[0] != num_blocks:
+        raise ValueError("kv_append: table sizes disagree")
+    need = int(lib.kv_append_workspace_size(S, num_blocks))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=k_new.device)
+    st = lib.kv_append(k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                       block_table.data_ptr(), seq_lens.data_ptr(), ref_counts.data_ptr(),
+                       free_ids.data_ptr(), free_top.data_ptr(), S, T, Hkv, d, num_blocks,
+                       block_table.shape[1], block_size, workspace.data_ptr(), workspace.numel(),
+                       _stream_handle(stream))
+    _check(st)
+
+
+def kv_append_workspace_size(num_seqs: int, num_blocks: int) -> int:
+    return int(load_library().kv_append_workspace_size(num_seqs, num_blocks))
 
 
 def device_status(stream=None) -> int:

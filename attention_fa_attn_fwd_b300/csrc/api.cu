@@ -219,6 +219,46 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   return ATTN_OK;
 }
 
+size_t kv_append_workspace_size(int num_seqs, int num_blocks) {
+  if (num_seqs < 1 || num_blocks < 1) return 0;
+  return attn::kv_append_workspace_bytes(num_seqs, num_blocks);
+}
+
+attn_status kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                      int32_t* block_table, int32_t* seq_lens, int32_t* ref_counts,
+                      const int32_t* free_ids, int32_t* free_top, int num_seqs, int T, int Hkv,
+                      int d, int num_blocks, int max_blocks_per_seq, int block_size,
+                      void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !seq_lens || !ref_counts ||
+      !free_ids || !free_top || !workspace)
+    return fail(ATTN_EINVAL, "kv_append: null pointer argument");
+  if (num_seqs < 1 || T < 1 || Hkv < 1 || num_blocks < 1 || max_blocks_per_seq < 1)
+    return fail(ATTN_EINVAL, "kv_append: sizes must be >= 1");
+  if (block_size != 16) return fail(ATTN_EINVAL, "kv_append: block_size must be 16");
+  if (d != 64 && d != 128) return fail(ATTN_EUNSUPPORTED, "kv_append: head dim %d", d);
+  if (num_seqs > 65535 || Hkv > 65535)
+    return fail(ATTN_EINVAL, "kv_append: num_seqs and Hkv must be <= 65535");
+  if ((long long)max_blocks_per_seq * 16 >= (1LL << 31) ||
+      (long long)num_blocks * 2 + (long long)num_seqs * 5 >= (1LL << 31))
+    return fail(ATTN_EINVAL, "kv_append: sizes too large");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      !aligned(ref_counts, 4) || !aligned(free_ids, 4) || !aligned(free_top, 4) ||
+      !aligned(workspace, 16))
+    return fail(ATTN_EINVAL, "kv_append: misaligned pointer");
+  const size_t need = attn::kv_append_workspace_bytes(num_seqs, num_blocks);
+  if (workspace_bytes < need)
+    return fail(ATTN_EINVAL, "kv_append: workspace %zu bytes < required %zu", workspace_bytes, need);
+  attn_status st = check_device();
+  if (st != ATTN_OK) return st;
+  cudaError_t e = attn::kv_append_launch(k_new, v_new, k_cache, v_cache, block_table, seq_lens,
+                                         ref_counts, free_ids, free_top, num_seqs, T, Hkv, d,
+                                         num_blocks, max_blocks_per_seq, workspace,
+                                         reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTN_ECUDA, "kv_append launch: %s", cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
 size_t paged_decode_workspace_size(int num_seqs, int H, int Hkv, int d, int max_blocks_per_seq) {
   if (num_seqs < 1 || H < 1 || Hkv < 1 || H % Hkv || max_blocks_per_seq < 1 || (d != 64 && d != 128))
     return 0;
@@ -267,9 +307,12 @@ attn_status attn_device_status(attn_stream_t stream) {
   const int a = attn::prefill_take_device_error();
   const int b = attn::decode_take_device_error();
   const int c = attn::backward_take_device_error();
-  if (a < 0 || b < 0 || c < 0) return fail(ATTN_ECUDA, "reading the device error word failed");
-  if (a || b || c)
-    return fail(ATTN_EDEVICE, "device error: prefill 0x%x, decode 0x%x, backward 0x%x", a, b, c);
+  const int f = attn::append_take_device_error();
+  if (a < 0 || b < 0 || c < 0 || f < 0)
+    return fail(ATTN_ECUDA, "reading the device error word failed");
+  if (a || b || c || f)
+    return fail(ATTN_EDEVICE, "device error: prefill 0x%x, decode 0x%x, backward 0x%x, append 0x%x",
+                a, b, c, f);
   return ATTN_OK;
 }
 

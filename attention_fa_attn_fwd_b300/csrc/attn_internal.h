@@ -47,6 +47,15 @@ cudaError_t backward_launch(const void* q, const void* k, const void* v, const v
                             void* workspace, cudaStream_t stream, const char** err);
 int backward_take_device_error();
 
+// ---- paged-cache append (kv_append.cu)
+size_t kv_append_workspace_bytes(int num_seqs, int num_blocks);
+cudaError_t kv_append_launch(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             int32_t* block_table, int32_t* seq_lens, int32_t* ref_counts,
+                             const int32_t* free_ids, int32_t* free_top, int num_seqs, int T,
+                             int Hkv, int d, int num_blocks, int max_blocks, void* workspace,
+                             cudaStream_t stream);
+int append_take_device_error();
+
 // Sets the calling thread's attn_last_error() message (printf-style).
 void set_last_error(const char* fmt, ...);
 

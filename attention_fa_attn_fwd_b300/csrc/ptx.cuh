@@ -23,6 +23,9 @@ enum : int {
   kErrDecodeBadBlock = 0x201,
   kErrPagedBadBlock = 0x202,   // paged prefill: block id outside [0, num_blocks)
   kErrPagedBadLength = 0x203,  // paged prefill: kv_lens[b] < 0 or > 16 * max_blocks
+  kErrAppendTable = 0x301,     // kv_append: length < 0 or the table is full
+  kErrAppendBlock = 0x302,     // kv_append: a table entry is not a block id
+  kErrAppendNoFree = 0x303,    // kv_append: not enough free blocks
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -382,6 +382,41 @@ def run_ours(args, ws, rank, local):
     pp_tflops = pp_flops / (pp_ms * 1e-3) / 1e12
     del pq, pkc, pvc, pbt, psl, po, plse
 
+    # ---- one decode step's KV append on the decode workload (beside the step)
+    nblk = [(int(n) + 15) // 16 for n in pb.seq_lens]
+    refs_h = torch.zeros(pb.num_blocks, dtype=torch.int32)
+    for s_ in range(pb.num_seqs):
+        for b_ in pb.block_table[s_, :nblk[s_]].tolist():
+            refs_h[b_] += 1
+    free_h = torch.nonzero(refs_h == 0).flatten().to(torch.int32)
+    a_bt, a_sl, a_rf = bt.clone(), sl.clone(), refs_h.to(dev)
+    a_free = free_h.to(dev)
+    a_top = torch.tensor([free_h.numel()], dtype=torch.int32, device=dev)
+    saved = (a_bt.clone(), a_sl.clone(), a_rf.clone(), a_top.clone())
+    g_ = torch.Generator().manual_seed(rank)
+    a_kn = torch.randn(pb.num_seqs, 1, kc.shape[1], kc.shape[3], generator=g_).to(torch.bfloat16).to(dev)
+    a_vn = torch.randn(a_kn.shape, generator=g_).to(torch.bfloat16).to(dev)
+    a_ws = torch.empty(binding.kv_append_workspace_size(pb.num_seqs, pb.num_blocks),
+                       dtype=torch.uint8, device=dev)
+    a_kc, a_vc = kc.clone(), vc.clone()
+
+    def kv_append_step():
+        binding.kv_append(a_kn, a_vn, a_kc, a_vc, a_bt, a_sl, a_rf, a_free, a_top,
+                          workspace=a_ws, stream=stream)
+
+    Ka = max(3, min(K, 100))
+    a_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ka + 3)]
+    for i in range(Ka + 3):
+        for dst_, src_ in zip((a_bt, a_sl, a_rf, a_top), saved):
+            dst_.copy_(src_)
+        a_evs[i][0].record(stream)
+        kv_append_step()
+        a_evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert binding.device_status(stream) == 0
+    ap_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in a_evs[3:]), ws)
+    del a_kc, a_vc
+
     # ---- backward pass of the prefill workload (reported beside the step)
     do_ = workloads.grad_output(q_h.shape, seed=rank).to(dev)
     dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -484,6 +519,9 @@ def run_ours(args, ws, rank, local):
                           "tflops": pp_tflops, "frac_burst": pp_tflops / ws / peak_tf,
                           "flops": pp_flops / ws, "kernel": "prefill_fwd_kernel<128, paged>",
                           "kv_lens": [int(x) for x in pp.seq_lens]},
+        "kv_append": {"workload": f"{DECODE}, one token per sequence", "us": 1e3 * ap_ms,
+                      "kernels": "kv_append_plan_kernel + kv_append_write_kernel<128>",
+                      "note": "latency-bound: 2 launches, 262 KB of new K/V rows"},
         "backward": {"workload": PREFILL, "ms": bw_ms, "tflops": bw_tflops,
                      "frac_burst": bw_tflops / ws / peak_tf,
                      "flops": bw_flops / ws, "flops_note": "algorithmic: 2.5 x forward (5 products)",

@@ -225,6 +225,57 @@ ATTN_API attn_status paged_prefill(const void* q, const void* k_cache, const voi
                                    int max_blocks_per_seq, int block_size, float scale, int causal,
                                    void* o, float* lse, attn_stream_t stream);
 
+/*
+ * kv_append_workspace_size -- bytes of device workspace kv_append needs
+ * (int32 scratch: 2 per pool block + 5 per sequence + 1).  0 for invalid
+ * sizes.  Pure host function.
+ */
+ATTN_API size_t kv_append_workspace_size(int num_seqs, int num_blocks);
+
+/*
+ * kv_append -- append T new tokens' K/V to every sequence of a paged cache,
+ * copying a shared block before writing into it (copy-on-write).
+ *
+ * Defined by: tutorial "第 3 章 进阶原理:性能模型与数值稳定性", section 3.0.6
+ * (PagedAttention: block table, sharing between sequences, copy-on-write)
+ * and 3.0.7 (block size 16; parallel sampling shares prefix blocks).  The
+ * pages name copy-on-write without detail; the reading implemented: sequence
+ * s's tokens seq_lens[s] .. seq_lens[s]+T-1 are written; a write into a block
+ * with ref_counts > 1 first copies that block into a fresh one (the table
+ * then points at the copy, the old block loses one reference), except that
+ * when every holder of the block is writing into it this step, the
+ * highest-numbered holder writes in place -- exactly what handling the
+ * sequences one at a time in index order gives.  Tokens that start a block
+ * take a fresh block.  Fresh blocks are popped off the free stack in sequence
+ * order: the a-th block taken this call is free_ids[*free_top - 1 - a].
+ *
+ *   k_new, v_new  [num_seqs, T, Hkv, d]               bf16 (read)
+ *   k_cache       [num_blocks, Hkv, 16, d]            bf16 (written)
+ *   v_cache       [num_blocks, Hkv, 16, d]            bf16 (written)
+ *   block_table   [num_seqs, max_blocks_per_seq]      int32 (updated)
+ *   seq_lens      [num_seqs]                          int32 (each += T)
+ *   ref_counts    [num_blocks]                        int32 (updated): number of
+ *                 (sequence, logical block) table entries holding each block
+ *   free_ids      [>= *free_top]                      int32 free block ids (read)
+ *   free_top      [1]                                 int32 stack height (updated)
+ *   workspace     >= kv_append_workspace_size(num_seqs, num_blocks) bytes,
+ *                 16-byte aligned; clobbered.
+ * All pointers are device pointers; nothing is read back to the host.  If a
+ * length is negative or would pass 16 * max_blocks_per_seq, a table entry to
+ * be written through is not a block id, or the stack holds too few blocks,
+ * nothing is modified and attn_device_status() reports the error.
+ *
+ * Requirements: block_size == 16; d in {64, 128}; num_seqs, Hkv <= 65535;
+ * k_new, v_new, caches and workspace 16-byte aligned.  Blocks in the stack
+ * must have ref_counts 0.
+ */
+ATTN_API attn_status kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                               int32_t* block_table, int32_t* seq_lens, int32_t* ref_counts,
+                               const int32_t* free_ids, int32_t* free_top, int num_seqs, int T,
+                               int Hkv, int d, int num_blocks, int max_blocks_per_seq,
+                               int block_size, void* workspace, size_t workspace_bytes,
+                               attn_stream_t stream);
+
 /* Message for the last non-OK status returned on the calling thread. */
 ATTN_API const char* attn_last_error(void);
 

@@ -29,7 +29,8 @@ def lib():
 def test_header_declares_expected_api():
     assert declared_functions() == sorted(["attn_fwd", "paged_decode", "paged_decode_workspace_size",
                                            "paged_decode_noalloc", "paged_prefill", "attn_bwd",
-                                           "attn_bwd_workspace_size", "attn_last_error",
+                                           "attn_bwd_workspace_size", "kv_append",
+                                           "kv_append_workspace_size", "attn_last_error",
                                            "attn_device_status"])
 
 
@@ -174,3 +175,28 @@ def test_bwd_workspace_size(lib):
     assert lib.attn_bwd_workspace_size(2, 16, 2048) == 2 * 16 * 2048 * 4
     assert lib.attn_bwd_workspace_size(1, 1, 1) == 256
     assert lib.attn_bwd_workspace_size(0, 1, 1) == 0
+
+
+def _app(lib, **kw):
+    a = dict(kn=_fake(1), vn=_fake(2), kc=_fake(3), vc=_fake(4), bt=_fake(5), sl=_fake(6),
+             rf=_fake(7), fi=_fake(8), ft=_fake(9), S=4, T=1, Hkv=8, d=128, nb=100, mb=64, bs=16,
+             ws=_fake(10), wsb=1 << 20, stream=None)
+    a.update(kw)
+    return lib.kv_append(a["kn"], a["vn"], a["kc"], a["vc"], a["bt"], a["sl"], a["rf"], a["fi"],
+                         a["ft"], a["S"], a["T"], a["Hkv"], a["d"], a["nb"], a["mb"], a["bs"],
+                         a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(rf=None), binding.ATTN_EINVAL),
+    (dict(ft=None), binding.ATTN_EINVAL),
+    (dict(T=0), binding.ATTN_EINVAL),
+    (dict(bs=32), binding.ATTN_EINVAL),
+    (dict(d=256), binding.ATTN_EUNSUPPORTED),
+    (dict(S=70000), binding.ATTN_EINVAL),
+    (dict(wsb=64), binding.ATTN_EINVAL),
+    (dict(kn=ctypes.c_void_p(0x10008)), binding.ATTN_EINVAL),
+])
+def test_kv_append_rejects_bad_arguments(lib, kw, status):
+    assert _app(lib, **kw) == status
+    assert lib.attn_last_error()
