@@ -28,10 +28,14 @@
 //
 // Warp roles in both tcgen05 kernels (12 warps): warp 0 TMA producer, warp 1
 // MMA issuer (one elected lane), warps 2-3 idle, warps 4-7 and 8-11 two
-// compute warpgroups that split the 128 score columns of every tile in
-// halves (thread r of a warpgroup owns TMEM lane / row r).  The compute
-// warpgroups write their bf16 results over the first 32 columns of their own
-// 64-column half, so the two never touch each other's columns.
+// compute warpgroups.  Every 128-wide score tile is split into two 64-wide
+// halves, one per compute warpgroup, each with its own TMEM buffer (S and dP
+// side by side, 64 columns each).  The MMA warp issues the next tile's
+// products for one half while the other half's warpgroup is still computing,
+// and the accumulating products (dQ, or dV and dK) of a half as soon as its
+// warpgroup has written its bf16 operands, so the tensor pipe and the
+// exponentials overlap.  A warpgroup writes its bf16 results over the first
+// 32 columns of the 64-column block they came from.
 
 #include <cmath>
 #include <cstdio>
@@ -59,13 +63,6 @@ struct BCfg {
 };
 
 // ---------------------------------------------------------------- helpers
-
-// TMEM column of the bf16 A operand for the MMA over K-slice kk (16
-// elements): the two compute warpgroups packed their 64-element halves into
-// columns [0, 32) and [64, 96) of a 128-column block.
-__device__ __forceinline__ uint32_t packed_col(int kk) {
-  return kk < 4 ? uint32_t(kk * 8) : uint32_t(64 + (kk - 4) * 8);
-}
 
 // 128-byte-swizzled row write of 32 fp32 values (scaled, rounded to bf16)
 // into a 128-row staging tile laid out in 64-column slabs.
@@ -132,7 +129,7 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restri
 template <int D>
 struct DqCfg : BCfg<D> {
   using B_ = BCfg<D>;
-  static constexpr int kKStages = (D == 128) ? 2 : 4;
+  static constexpr int kKStages = (D == 128) ? 3 : 4;
   static constexpr int kVStages = (D == 128) ? 2 : 3;
   static constexpr int kOffQ = 0;
   static constexpr int kOffDO = B_::kTileBytes;
@@ -144,14 +141,15 @@ struct DqCfg : BCfg<D> {
   static constexpr int kBarKE = kBarKF + kKStages;
   static constexpr int kBarVF = kBarKE + kKStages;
   static constexpr int kBarVE = kBarVF + kVStages;
-  static constexpr int kBarSF = kBarVE + kVStages;  // S and dP in TMEM
-  static constexpr int kBarPF = kBarSF + 1;         // dS written (256 arrivals)
-  static constexpr int kBarOF = kBarPF + 1;         // dQ complete
+  static constexpr int kBarSF = kBarVE + kVStages;  // 2: S_h and dP_h of half h in TMEM
+  static constexpr int kBarPF = kBarSF + 2;         // 2: dS_h written (128 arrivals each)
+  static constexpr int kBarOF = kBarPF + 2;         // dQ complete
   static constexpr int kBarDrain = kBarOF + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  // half h: S_h at h*128 (64 columns), dP_h at h*128 + 64; dQ at 256.
+  static constexpr uint32_t kColDQ = 256;
 };
 
 template <int D>
@@ -183,7 +181,8 @@ __global__ void __launch_bounds__(384, 1)
   const int n = (kv_end > 0 && !dead) ? (kv_end + 127) / 128 : 0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kNumBars; ++i) mbar_init(bar(i), i == C::kBarPF ? 256u : 1u);
+    for (int i = 0; i < C::kNumBars; ++i)
+      mbar_init(bar(i), (i == C::kBarPF || i == C::kBarPF + 1) ? 128u : 1u);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -244,15 +243,51 @@ __global__ void __launch_bounds__(384, 1)
       }
     } else if (warp == 1 && n > 0) {
       // ------------------------------------------------------ MMA issuer
-      constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, 0);
+      constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, 0);
       constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, 1);
       const uint64_t q_desc = smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
       const uint64_t do_desc = smem_desc_sw128(sbase + C::kOffDO, 16, 1024);
       const uint64_t k_desc = smem_desc_sw128(sbase + C::kOffK, 16, 1024);
       const uint64_t v_desc = smem_desc_sw128(sbase + C::kOffV, 16, 1024);
       const uint64_t kmn_desc = smem_desc_sw128(sbase + C::kOffK, C::kSlabBytes, 1024);
+      // S_h = Q K_j[h]^T and dP_h = dO V_j[h]^T over keys h*64 .. h*64+63
+      // (64 rows further into the K / V tile: +8 KB per slab).
+      auto issue_s_dp = [&](int h, int ks, int vs) {
+        const uint64_t ko = uint64_t((ks * C::kTileBytes + h * 8192) >> 4);
+        const uint64_t vo = uint64_t((vs * C::kTileBytes + h * 8192) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + h * 128, q_desc + off, k_desc + ko + off, kIdescHalf,
+                      kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + h * 128 + 64, do_desc + off, v_desc + vo + off, kIdescHalf,
+                      kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBarSF + h));
+      };
+      // dQ += dS_h K_j[h]: A = dS_h (bf16 in TMEM), 16 keys per MMA.
+      auto issue_dq = [&](int h, int j) -> bool {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF + h), j & 1, abort_flag, err,
+                                               kErrTimeoutMma)))
+          return false;
+        tc_fence_after();
+        const int ks = j % C::kKStages;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ts(tmem + C::kColDQ, tmem + h * 128 + kk * 8,
+                      kmn_desc + uint64_t((ks * C::kTileBytes + (h * 64 + kk * 16) * 128) >> 4),
+                      kIdescDQ, (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
+        if (h == 1) mma_commit(bar(C::kBarKE + ks));
+        return true;
+      };
       bool ok = __all_sync(0xffffffffu,
                            mbar_wait(bar(C::kBarQF), 0, abort_flag, err, kErrTimeoutMma));
+      // Issue order: S/dP(j,0) [dQ(j-1,1)] S/dP(j,1) dQ(j,0), so one half's
+      // products run while the other half's warpgroup computes.
       for (int j = 0; ok && j < n; ++j) {
         const int ks = j % C::kKStages, vs = j % C::kVStages;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarKF + ks), (j / C::kKStages) & 1,
@@ -262,32 +297,16 @@ __global__ void __launch_bounds__(384, 1)
                                                abort_flag, err, kErrTimeoutMma));
         if (!ok) break;
         tc_fence_after();
-        const uint64_t ko = uint64_t((ks * C::kTileBytes) >> 4);
-        const uint64_t vo = uint64_t((vs * C::kTileBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // S = Q K_j^T
-          const uint64_t off = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tmem + C::kColS, q_desc + off, k_desc + ko + off, kIdescSS, kk > 0 ? 1u : 0u);
+        issue_s_dp(0, ks, vs);
+        if (j > 0) {
+          ok = issue_dq(1, j - 1);
+          if (!ok) break;
         }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V_j^T
-          const uint64_t off = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tmem + C::kColDP, do_desc + off, v_desc + vo + off, kIdescSS,
-                      kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(C::kBarSF));
+        issue_s_dp(1, ks, vs);
         mma_commit(bar(C::kBarVE + vs));
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar(C::kBarPF), j & 1, abort_flag, err, kErrTimeoutMma));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j (16 keys per MMA)
-          mma_bf16_ts(tmem + C::kColDQ, tmem + C::kColS + packed_col(kk),
-                      kmn_desc + ko + uint64_t((kk * 2048) >> 4), kIdescDQ,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(C::kBarKE + ks));
+        ok = issue_dq(0, j);
       }
+      if (ok && n > 0) ok = issue_dq(1, n - 1);
       if (ok) {
         mma_commit(bar(C::kBarOF));
       } else {
@@ -313,14 +332,14 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = !dead;
     for (int j = 0; ok && j < n; ++j) {
       ok = __all_sync(0xffffffffu,
-                      mbar_wait(bar(C::kBarSF), j & 1, abort_flag, err, kErrTimeoutSoftmax));
+                      mbar_wait(bar(C::kBarSF + wg), j & 1, abort_flag, err, kErrTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after();
       uint32_t s[64], p[64];
-      tmem_ld32(lane_base + C::kColS + wg * 64, s);
-      tmem_ld32(lane_base + C::kColS + wg * 64 + 32, s + 32);
-      tmem_ld32(lane_base + C::kColDP + wg * 64, p);
-      tmem_ld32(lane_base + C::kColDP + wg * 64 + 32, p + 32);
+      tmem_ld32(lane_base + wg * 128, s);
+      tmem_ld32(lane_base + wg * 128 + 32, s + 32);
+      tmem_ld32(lane_base + wg * 128 + 64, p);
+      tmem_ld32(lane_base + wg * 128 + 96, p + 32);
       tmem_ld_wait();
       reg_fence<64>(s);
       reg_fence<64>(p);
@@ -336,10 +355,10 @@ __global__ void __launch_bounds__(384, 1)
         const float d1 = x1 * (__uint_as_float(p[2 * e + 1]) - drow);
         pk[e] = pack_bf16x2(d0, d1);
       }
-      tmem_st32(lane_base + C::kColS + wg * 64, pk);
+      tmem_st32(lane_base + wg * 128, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::kBarPF));
+      mbar_arrive(bar(C::kBarPF + wg));
     }
     // -------------------------------------------------------- epilogue
     if (ok && n > 0) {
@@ -396,14 +415,15 @@ struct DkvCfg : BCfg<D> {
   static constexpr int kBarKVF = 0;
   static constexpr int kBarQF = 1;
   static constexpr int kBarQE = kBarQF + kQStages;
-  static constexpr int kBarSF = kBarQE + kQStages;  // S^T and dP^T in TMEM
-  static constexpr int kBarPF = kBarSF + 1;         // P^T, dS^T written (256 arrivals)
-  static constexpr int kBarOF = kBarPF + 1;         // dK, dV complete
+  static constexpr int kBarSF = kBarQE + kQStages;  // 2: S^T_h and dP^T_h in TMEM
+  static constexpr int kBarPF = kBarSF + 2;         // 2: P^T_h, dS^T_h written (128 each)
+  static constexpr int kBarOF = kBarPF + 2;         // dK, dV complete
   static constexpr int kBarDrain = kBarOF + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  // half h: S^T_h at h*128 (64 columns), dP^T_h at h*128 + 64; dV, dK after.
+  static constexpr uint32_t kColDV = 256, kColDK = 256 + D;
 };
 
 template <int D>
@@ -424,10 +444,12 @@ __global__ void __launch_bounds__(384, 1)
   int* err = &g_backward_error;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // CTA = (KV tile, b, KV head); causal: early key tiles (most query tiles) first.
-  const int BK = a.B * a.Hkv;
-  const int zkv = blockIdx.x % BK;
-  const int k0 = int(blockIdx.x / BK) * 128;
+  // CTA = (b, KV head, KV tile), KV tiles of one head adjacent so resident
+  // CTAs share that group's Q / dO in L2; causal: early key tiles (the ones
+  // most query tiles attend) first within a head.
+  const int n_kt = (a.Nk + 127) / 128;
+  const int zkv = blockIdx.x / n_kt;
+  const int k0 = int(blockIdx.x % n_kt) * 128;
   const int b = zkv / a.Hkv, g = zkv % a.Hkv;
   const int G = a.H / a.Hkv;
   const int off = a.Nk - a.Nq;  // query row i sees keys j <= i + off (causal)
@@ -444,7 +466,7 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) {
       uint32_t cnt = 1;
-      if (i == C::kBarPF) cnt = 256;
+      if (i == C::kBarPF || i == C::kBarPF + 1) cnt = 128;
       if (i >= C::kBarQF && i < C::kBarQF + C::kQStages) cnt = 32;
       mbar_init(bar(i), cnt);
     }
@@ -523,7 +545,7 @@ __global__ void __launch_bounds__(384, 1)
       }
     } else if (warp == 1 && n_it > 0) {
       // ------------------------------------------------------ MMA issuer
-      constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, 0);
+      constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, 0);
       constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 1);
       const uint64_t k_desc = smem_desc_sw128(sbase + C::kOffK, 16, 1024);
       const uint64_t v_desc = smem_desc_sw128(sbase + C::kOffV, 16, 1024);
@@ -531,41 +553,59 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t do_desc = smem_desc_sw128(sbase + C::kOffDO, 16, 1024);
       const uint64_t qmn_desc = smem_desc_sw128(sbase + C::kOffQ, C::kSlabBytes, 1024);
       const uint64_t domn_desc = smem_desc_sw128(sbase + C::kOffDO, C::kSlabBytes, 1024);
+      // S^T_h = K Q[h]^T, dP^T_h = V dO[h]^T over queries h*64 .. h*64+63.
+      auto issue_s_dp = [&](int h, int st) {
+        const uint64_t so = uint64_t((st * C::kTileBytes + h * 8192) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t o16 = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + h * 128, k_desc + o16, q_desc + so + o16, kIdescHalf,
+                      kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t o16 = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + h * 128 + 64, v_desc + o16, do_desc + so + o16, kIdescHalf,
+                      kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBarSF + h));
+      };
+      // dV += P^T_h dO[h], dK += dS^T_h Q[h] (16 queries per MMA).
+      auto issue_acc = [&](int h, int it) -> bool {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF + h), it & 1, abort_flag, err,
+                                               kErrTimeoutMma)))
+          return false;
+        tc_fence_after();
+        const int st = it % C::kQStages;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t o16 = uint64_t((st * C::kTileBytes + (h * 64 + kk * 16) * 128) >> 4);
+          const uint32_t acc = (it > 0 || h > 0 || kk > 0) ? 1u : 0u;
+          mma_bf16_ts(tmem + C::kColDV, tmem + h * 128 + kk * 8, domn_desc + o16, kIdescAcc, acc);
+          mma_bf16_ts(tmem + C::kColDK, tmem + h * 128 + 64 + kk * 8, qmn_desc + o16, kIdescAcc,
+                      acc);
+        }
+        if (h == 1) mma_commit(bar(C::kBarQE + st));
+        return true;
+      };
       bool ok = __all_sync(0xffffffffu,
                            mbar_wait(bar(C::kBarKVF), 0, abort_flag, err, kErrTimeoutMma));
+      // Issue order: S/dP(it,0) [acc(it-1,1)] S/dP(it,1) acc(it,0).
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it % C::kQStages;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarQF + st), (it / C::kQStages) & 1,
                                                abort_flag, err, kErrTimeoutMma));
         if (!ok) break;
         tc_fence_after();
-        const uint64_t so = uint64_t((st * C::kTileBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K Q^T, dP^T = V dO^T
-          const uint64_t o16 = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tmem + C::kColS, k_desc + o16, q_desc + so + o16, kIdescSS, kk > 0 ? 1u : 0u);
+        issue_s_dp(0, st);
+        if (it > 0) {
+          ok = issue_acc(1, it - 1);
+          if (!ok) break;
         }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t o16 = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tmem + C::kColDP, v_desc + o16, do_desc + so + o16, kIdescSS,
-                      kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(C::kBarSF));
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar(C::kBarPF), it & 1, abort_flag, err, kErrTimeoutMma));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // dV += P^T dO, dK += dS^T Q (16 queries per MMA)
-          const uint64_t o16 = so + uint64_t((kk * 2048) >> 4);
-          mma_bf16_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(kk), domn_desc + o16,
-                      kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
-          mma_bf16_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col(kk), qmn_desc + o16,
-                      kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(C::kBarQE + st));
+        issue_s_dp(1, st);
+        ok = issue_acc(0, it);
       }
+      if (ok && n_it > 0) ok = issue_acc(1, n_it - 1);
       if (ok) {
         mma_commit(bar(C::kBarOF));
       } else {
@@ -590,14 +630,14 @@ __global__ void __launch_bounds__(384, 1)
                                              abort_flag, err, kErrTimeoutSoftmax));
       if (!ok) break;
       ok = __all_sync(0xffffffffu,
-                      mbar_wait(bar(C::kBarSF), it & 1, abort_flag, err, kErrTimeoutSoftmax));
+                      mbar_wait(bar(C::kBarSF + wg), it & 1, abort_flag, err, kErrTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after();
       uint32_t s[64], p[64];
-      tmem_ld32(lane_base + C::kColS + wg * 64, s);
-      tmem_ld32(lane_base + C::kColS + wg * 64 + 32, s + 32);
-      tmem_ld32(lane_base + C::kColDP + wg * 64, p);
-      tmem_ld32(lane_base + C::kColDP + wg * 64 + 32, p + 32);
+      tmem_ld32(lane_base + wg * 128, s);
+      tmem_ld32(lane_base + wg * 128 + 32, s + 32);
+      tmem_ld32(lane_base + wg * 128 + 64, p);
+      tmem_ld32(lane_base + wg * 128 + 96, p + 32);
       tmem_ld_wait();
       reg_fence<64>(s);
       reg_fence<64>(p);
@@ -618,11 +658,11 @@ __global__ void __launch_bounds__(384, 1)
         pd[e] = pack_bf16x2(x0 * (__uint_as_float(p[2 * e]) - dd[2 * e]),
                             x1 * (__uint_as_float(p[2 * e + 1]) - dd[2 * e + 1]));
       }
-      tmem_st32(lane_base + C::kColS + wg * 64, pp);
-      tmem_st32(lane_base + C::kColDP + wg * 64, pd);
+      tmem_st32(lane_base + wg * 128, pp);
+      tmem_st32(lane_base + wg * 128 + 64, pd);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::kBarPF));
+      mbar_arrive(bar(C::kBarPF + wg));
     }
     // -------------------------------------------------------- epilogue
     if (ok && n_it > 0) {

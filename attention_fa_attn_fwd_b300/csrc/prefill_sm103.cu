@@ -112,6 +112,7 @@ struct Args {
   const int32_t* kv_lens;      // [B]
   int max_blocks, num_blocks;
   int oob_row;                 // a pool row past the end: TMA fills zeros
+  int group_major;             // CTA order (see the kernel)
 };
 
 constexpr int kPageTokens = 16;  // PagedAttention block size
@@ -136,9 +137,22 @@ __global__ void __launch_bounds__(384, 1)
   const int lane = threadIdx.x & 31;
 
   // Heavy (late, causal) tile pairs first; heads of one KV group adjacent.
+  // group_major: all tile pairs of one (batch, KV head) group before the
+  // next group, so the CTAs resident at once share one group's K/V in L2
+  // (used when all groups' K/V would not fit in L2 together).
   const int BH = a.B * a.H;
-  const int bh = blockIdx.x % BH;
-  const int q0 = (a.n_pairs - 1 - int(blockIdx.x / BH)) * 256;
+  int bh, pair;
+  if (a.group_major) {
+    const int G = a.H / a.Hkv;
+    const int per_group = a.n_pairs * G;
+    const int grp = blockIdx.x / per_group, r = blockIdx.x % per_group;
+    pair = r / G;
+    bh = grp * G + r % G;
+  } else {
+    bh = blockIdx.x % BH;
+    pair = blockIdx.x / BH;
+  }
+  const int q0 = (a.n_pairs - 1 - pair) * 256;
   const int b = bh / a.H;
   const int h = bh % a.H;
   const int g_kv = h / (a.H / a.Hkv);
@@ -579,6 +593,8 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
   a.n_pairs = (Nq + 255) / 256;
   a.c_log2 = scale * kLog2e;
   a.causal = causal;
+  // K + V of every group at once above ~96 MB would thrash the 126 MB L2.
+  a.group_major = (uint64_t(B) * Hkv * Nk * D * 4 > (96ull << 20)) ? 1 : 0;
   const unsigned grid = unsigned(a.n_pairs) * unsigned(B) * unsigned(H);
   prefill_fwd_kernel<D, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
@@ -617,6 +633,7 @@ cudaError_t launch_paged(const void* q, const void* k_cache, const void* v_cache
   a.max_blocks = max_blocks;
   a.num_blocks = num_blocks;
   a.oob_row = int(rows);
+  a.group_major = 1;  // sequences have their own caches: keep one group's in L2
   const unsigned grid = unsigned(a.n_pairs) * unsigned(B) * unsigned(H);
   prefill_fwd_kernel<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
