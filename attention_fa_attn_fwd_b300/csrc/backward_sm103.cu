@@ -56,7 +56,6 @@ struct BCfg {
   static constexpr int kSlabs = D / 64;
   static constexpr int kSlabBytes = 128 * 128;             // 128 rows x 64 bf16
   static constexpr int kTileBytes = kSlabs * kSlabBytes;   // one 128-row tile
-  static constexpr int kThreads = 384;
   static constexpr int kRegsLow = 80;
   static constexpr int kRegsHigh = 208;
   static constexpr uint32_t kTmemCols = 512;

@@ -18,7 +18,8 @@
 // warps merge in shared memory and write one unnormalised partial
 // (o, m, l) per head to the workspace.
 //
-// Kernel 2 (merge): per (sequence, head), combine the splits by their LSE:
+// Kernel 2 (merge, a programmatic dependent launch so its start overlaps the
+// split kernel's tail): per (sequence, head), combine the splits by their LSE:
 // M = max m_r, L = sum 2^(m_r - M) l_r, o = sum 2^(m_r - M) o_r / L,
 // lse = (M + log2 L) ln 2.  Deterministic order, no atomics.
 
@@ -97,6 +98,9 @@ __global__ void __launch_bounds__(128)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + kWarps * kRing * 8);
   int* err = &g_decode_error;
 
+  // The merge kernel may be scheduled once every CTA of this grid has
+  // started; it waits for this grid's completion before reading partials.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int seq_len = a.seq_lens[s];
@@ -318,34 +322,62 @@ __global__ void __launch_bounds__(128)
   }
 }
 
-// One warp per (sequence, head).
+// One warp per (sequence, head).  Launched as a programmatic dependent of the
+// split kernel: its CTAs may start while the split kernel's last wave runs and
+// wait (griddepcontrol.wait) until every partial is written and visible.
+// Lane r loads split r's (m, l), so the weights take one round trip; the
+// partial outputs are then summed with independent loads.
 template <int D>
 __global__ void __launch_bounds__(256)
     decode_merge_kernel(const DArgs a, uint16_t* __restrict__ o, float* __restrict__ lse,
                         int num_seqs) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (gw >= num_seqs * a.H) return;
   const int s = gw / a.H;
   const int seq_len = a.seq_lens[s];
   const int nblk = min((max(seq_len, 0) + kBlockTokens - 1) / kBlockTokens, a.max_blocks);
   const int nsp = (nblk + a.bps - 1) / a.bps;
   const size_t head = size_t(gw);
+  const float* ml = a.ws_ml + head * a.max_splits * 2;
   float M = -INFINITY;
-  for (int r = 0; r < nsp; ++r) M = fmaxf(M, a.ws_ml[(head * a.max_splits + r) * 2]);
+  for (int r = lane; r < nsp; r += 32) M = fmaxf(M, ml[2 * r]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   constexpr int PER = D / 32;
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float L = 0.f;
-  for (int r = 0; r < nsp; ++r) {
-    const float mr = a.ws_ml[(head * a.max_splits + r) * 2];
-    const float w = (mr == -INFINITY) ? 0.f : ex2_approx(mr - M);
-    L += w * a.ws_ml[(head * a.max_splits + r) * 2 + 1];
-    const float* src = a.ws_o + (head * a.max_splits + r) * D + lane * PER;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] += w * src[e];
+  for (int r0 = 0; r0 < nsp; r0 += 32) {
+    // weights of splits r0 .. r0+31, one per lane
+    float w_mine = 0.f;
+    if (r0 + lane < nsp) {
+      const float mr = ml[2 * (r0 + lane)];
+      w_mine = (mr == -INFINITY) ? 0.f : ex2_approx(mr - M);
+      L += w_mine * ml[2 * (r0 + lane) + 1];
+    }
+    const int cnt = min(32, nsp - r0);
+    const float* src = a.ws_o + (head * a.max_splits + r0) * D + lane * PER;
+#pragma unroll 4
+    for (int r = 0; r < cnt; ++r) {
+      const float w = __shfl_sync(0xffffffffu, w_mine, r);
+      if constexpr (PER == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src + size_t(r) * D);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+        acc[2] += w * v.z;
+        acc[3] += w * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src + size_t(r) * D);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+      }
+    }
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
   uint16_t* dst = o + head * D + lane * PER;
 #pragma unroll
@@ -397,8 +429,17 @@ cudaError_t launch(const void* q, const void* k_cache, const void* v_cache, cons
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = S * H;
-  decode_merge_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(a, static_cast<uint16_t*>(o), lse, S);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((warps + 7) / 8);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, a, static_cast<uint16_t*>(o), lse, S);
 }
 
 }  // namespace

@@ -10,8 +10,8 @@ N16384 d128; 335 MB on the device, larger than L2).  ``decode``: paged_decode
 on the 64-sequence workload (2.3 GB pool).  ``step``: both, as one bench step.
 ``paged_prefill``: chunked prefill of 8 x 2048 tokens over a paged cache.
 ``backward``: attn_bwd on the prefill workload (after one untimed attn_fwd).
-A 256 MiB L2 flush (a memset, not one of this library's kernels) precedes
-every kernel, as in bench.py.  Prints the CUDA-event time of each launch.
+An L2 flush (``measure.L2Flush``: torch kernels, not this library's)
+precedes every kernel, as in bench.py.  Prints the CUDA-event time of each launch.
 """
 
 from __future__ import annotations
@@ -22,6 +22,7 @@ import math
 import torch
 
 from . import binding, workloads
+from .measure import L2Flush
 
 
 def main(argv=None):
@@ -34,7 +35,7 @@ def main(argv=None):
     args = ap.parse_args(argv)
     binding.load_library()
     dev = torch.device("cuda", 0)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     runs = []
     if args.case in ("prefill", "step"):
         cfg = dict(workloads.PREFILL_WORKLOADS.get(args.prefill) or workloads.sweep_workloads()[args.prefill])
@@ -76,7 +77,7 @@ def main(argv=None):
                                                           dq=dq, dk=dk, dv=dv, workspace=bws)))
     for it in range(args.iters):
         for name, fn in runs:
-            flush.zero_()
+            flush()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record()

@@ -9,7 +9,8 @@ A step is one pass of the whole hot path over one batch of synthetic input:
 ``value`` is the prefill throughput in TFLOP/s (FLOPs = 4*B*H*Nq*Nk*d, halved
 for causal); the decode throughput (KV GB/s over the unique bytes read) is
 reported beside it.  Kernel times are CUDA events on the launching stream,
-with a 256 MiB L2 flush (outside the events) before every kernel.
+with an L2 flush (outside the events) before every kernel: a 256 MiB write,
+then a 256 MiB read so the lines left in L2 are clean (``measure.L2Flush``).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -38,12 +39,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from attention_fa_attn_fwd_b300 import workloads  # noqa: E402
+from attention_fa_attn_fwd_b300.measure import L2Flush  # noqa: E402
 
 PREFILL = "gqa_b1h32kv8_n16384_d128_causal"
 DECODE = "paged_decode_s64_h32kv8_d128"
 PAGED_PREFILL = "paged_prefill_s8_h32kv8_q2048_d128"
 METRIC = "prefill attn TFLOP/s & % BF16 tensor peak; paged decode KV GB/s & % HBM"
-FLUSH_BYTES = 256 << 20
 
 
 def load_peaks():
@@ -298,7 +299,7 @@ def run_ours(args, ws, rank, local):
     wsb = binding.paged_decode_workspace_size(dq.shape[0], dq.shape[1], kc.shape[1], dq.shape[2],
                                               bt.shape[1])
     wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
 
     def prefill():
@@ -308,9 +309,9 @@ def run_ours(args, ws, rank, local):
         binding.paged_decode(dq, kc, vc, bt, sl, o=do, lse=dlse, workspace=wsp, stream=stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         prefill()
-        flush.zero_()
+        flush()
         decode()
     torch.cuda.synchronize()
     assert binding.device_status(stream) == 0
@@ -324,11 +325,11 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     t0 = time.time()
     for i in range(K):
-        flush.zero_()
+        flush()
         evs[i][0].record(stream)
         prefill()
         evs[i][1].record(stream)
-        flush.zero_()
+        flush()
         evs[i][2].record(stream)
         decode()
         evs[i][3].record(stream)
@@ -366,12 +367,12 @@ def run_ours(args, ws, rank, local):
         binding.paged_prefill(pq, pkc, pvc, pbt, psl, causal=True, o=po, lse=plse, stream=stream)
 
     for _ in range(3):
-        flush.zero_()
+        flush()
         paged_prefill()
     Kp = max(3, min(K, 100))
     p_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kp)]
     for i in range(Kp):
-        flush.zero_()
+        flush()
         p_evs[i][0].record(stream)
         paged_prefill()
         p_evs[i][1].record(stream)
@@ -382,40 +383,64 @@ def run_ours(args, ws, rank, local):
     pp_tflops = pp_flops / (pp_ms * 1e-3) / 1e12
     del pq, pkc, pvc, pbt, psl, po, plse
 
-    # ---- one decode step's KV append on the decode workload (beside the step)
+    # ---- KV append for a run of decode steps (reported beside the step).
+    # One append is two tiny launches, far shorter than the host-side call, so
+    # a run of APPEND_STEPS appends is captured once as a CUDA graph and the
+    # replay is timed; the table gets spare columns so no sequence overflows.
+    APPEND_STEPS = 16
     nblk = [(int(n) + 15) // 16 for n in pb.seq_lens]
     refs_h = torch.zeros(pb.num_blocks, dtype=torch.int32)
     for s_ in range(pb.num_seqs):
         for b_ in pb.block_table[s_, :nblk[s_]].tolist():
             refs_h[b_] += 1
     free_h = torch.nonzero(refs_h == 0).flatten().to(torch.int32)
-    a_bt, a_sl, a_rf = bt.clone(), sl.clone(), refs_h.to(dev)
+    bt_wide = torch.zeros(pb.num_seqs, pb.max_blocks_per_seq + 2, dtype=torch.int32)
+    bt_wide[:, :pb.max_blocks_per_seq] = pb.block_table
+    a_bt, a_sl, a_rf = bt_wide.to(dev), sl.clone(), refs_h.to(dev)
     a_free = free_h.to(dev)
     a_top = torch.tensor([free_h.numel()], dtype=torch.int32, device=dev)
     saved = (a_bt.clone(), a_sl.clone(), a_rf.clone(), a_top.clone())
     g_ = torch.Generator().manual_seed(rank)
-    a_kn = torch.randn(pb.num_seqs, 1, kc.shape[1], kc.shape[3], generator=g_).to(torch.bfloat16).to(dev)
+    a_kn = torch.randn(APPEND_STEPS, pb.num_seqs, 1, kc.shape[1], kc.shape[3],
+                       generator=g_).to(torch.bfloat16).to(dev)
     a_vn = torch.randn(a_kn.shape, generator=g_).to(torch.bfloat16).to(dev)
     a_ws = torch.empty(binding.kv_append_workspace_size(pb.num_seqs, pb.num_blocks),
                        dtype=torch.uint8, device=dev)
     a_kc, a_vc = kc.clone(), vc.clone()
 
-    def kv_append_step():
-        binding.kv_append(a_kn, a_vn, a_kc, a_vc, a_bt, a_sl, a_rf, a_free, a_top,
-                          workspace=a_ws, stream=stream)
-
-    Ka = max(3, min(K, 100))
-    a_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ka + 3)]
-    for i in range(Ka + 3):
+    def restore():
         for dst_, src_ in zip((a_bt, a_sl, a_rf, a_top), saved):
             dst_.copy_(src_)
+
+    def append_run():
+        for i_ in range(APPEND_STEPS):
+            binding.kv_append(a_kn[i_], a_vn[i_], a_kc, a_vc, a_bt, a_sl, a_rf, a_free, a_top,
+                              workspace=a_ws)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        restore()
+        append_run()  # warm-up outside capture (first-call device queries)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        append_run()
+    Ka = max(3, min(K, 50))
+    a_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ka)]
+    for i in range(Ka):
+        restore()
+        flush()
         a_evs[i][0].record(stream)
-        kv_append_step()
+        graph.replay()
         a_evs[i][1].record(stream)
     torch.cuda.synchronize()
     assert binding.device_status(stream) == 0
-    ap_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in a_evs[3:]), ws)
-    del a_kc, a_vc
+    assert int(a_sl[0]) == int(saved[1][0]) + APPEND_STEPS
+    ap_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in a_evs), ws)
+    ap_ms /= APPEND_STEPS
+    del a_kc, a_vc, graph
 
     # ---- backward pass of the prefill workload (reported beside the step)
     do_ = workloads.grad_output(q_h.shape, seed=rank).to(dev)
@@ -429,12 +454,12 @@ def run_ours(args, ws, rank, local):
                          workspace=bws, stream=stream)
 
     for _ in range(3):
-        flush.zero_()
+        flush()
         backward()
     Kb = max(3, min(K, 50))
     b_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kb)]
     for i in range(Kb):
-        flush.zero_()
+        flush()
         b_evs[i][0].record(stream)
         backward()
         b_evs[i][1].record(stream)
@@ -458,7 +483,7 @@ def run_ours(args, ws, rank, local):
     e_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(Ke)]
 
     def e2e_step(ev):
-        flush.zero_()
+        flush()
         if ev:
             ev[0].record(stream)
         q.copy_(qp, non_blocking=True)
@@ -500,7 +525,8 @@ def run_ours(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": p_mean + d_mean, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{PREFILL} + {DECODE}", "prefill": cfg, "decode": dcfg,
-                   "l2": "256 MiB L2 flush before every kernel (outside the events)",
+                   "l2": "L2 flush before every timed kernel, outside the events: write 256 MiB, "
+                         "then read 256 MiB (clean lines)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "prefill": {"ms": p_mean, "tflops": tflops, "frac_burst": k_tflops / peak_tf,
                     "frac_sustained": k_tflops / peaks["bf16_tflops_sustained"]},
@@ -519,9 +545,11 @@ def run_ours(args, ws, rank, local):
                           "tflops": pp_tflops, "frac_burst": pp_tflops / ws / peak_tf,
                           "flops": pp_flops / ws, "kernel": "prefill_fwd_kernel<128, paged>",
                           "kv_lens": [int(x) for x in pp.seq_lens]},
-        "kv_append": {"workload": f"{DECODE}, one token per sequence", "us": 1e3 * ap_ms,
+        "kv_append": {"workload": f"{DECODE}, one token per sequence per step",
+                      "us_per_step": 1e3 * ap_ms,
                       "kernels": "kv_append_plan_kernel + kv_append_write_kernel<128>",
-                      "note": "latency-bound: 2 launches, 262 KB of new K/V rows"},
+                      "note": f"CUDA graph of {APPEND_STEPS} decode-step appends, time / steps; "
+                              "latency-bound: 2 launches, 262 KB of new K/V rows per step"},
         "backward": {"workload": PREFILL, "ms": bw_ms, "tflops": bw_tflops,
                      "frac_burst": bw_tflops / ws / peak_tf,
                      "flops": bw_flops / ws, "flops_note": "algorithmic: 2.5 x forward (5 products)",
