@@ -25,6 +25,7 @@ ATTN_EINVAL = 1
 ATTN_EUNSUPPORTED = 2
 ATTN_ECUDA = 3
 ATTN_EDEVICE = 4
+ATTN_FWD_EXP2_FMA = 1  # attn_fwd_ex flag
 _STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_EINVAL", 2: "ATTN_EUNSUPPORTED",
                  3: "ATTN_ECUDA", 4: "ATTN_EDEVICE"}
 
@@ -35,6 +36,8 @@ _f = ctypes.c_float
 _sz = ctypes.c_size_t
 SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "attn_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, ctypes.c_uint,
+                         _vp]),
     "paged_decode_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "paged_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                           _vp, _vp, _vp, _sz, _vp]),
@@ -108,11 +111,13 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
              causal: bool = False, scale: Optional[float] = None,
              o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-             want_lse: bool = True, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+             want_lse: bool = True, stream=None,
+             exp2_fma: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """O = softmax(scale Q K^T [causal]) V and per-row LSE via ``attn_fwd``.
 
     q [B,H,Nq,d], k/v [B,Hkv,Nk,d], bf16, contiguous, on one CUDA device.
     Returns (o [B,H,Nq,d] bf16, lse [B,H,Nq] fp32 or None).
+    ``exp2_fma=True`` calls ``attn_fwd_ex`` with ATTN_FWD_EXP2_FMA.
     """
     lib = load_library()
     _need(q, "q", torch.bfloat16, 4)
@@ -136,10 +141,16 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         _need(lse, "lse", torch.float32, 3)
         if tuple(lse.shape) != (B, H, Nq):
             raise ValueError("lse must be [B, H, Nq]")
-    st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                      lse.data_ptr() if lse is not None else None,
-                      B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
-                      _stream_handle(stream))
+    if exp2_fma:
+        st = lib.attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                             lse.data_ptr() if lse is not None else None,
+                             B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                             ATTN_FWD_EXP2_FMA, _stream_handle(stream))
+    else:
+        st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                          lse.data_ptr() if lse is not None else None,
+                          B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                          _stream_handle(stream))
     _check(st)
     return o, lse
 

@@ -116,9 +116,9 @@ extern "C" {
 
 const char* attn_last_error(void) { return g_msg; }
 
-attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                     int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
-                     attn_stream_t stream) {
+attn_status attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                        unsigned flags, attn_stream_t stream) {
   if (!q || !k || !v || !o) return fail(ATTN_EINVAL, "attn_fwd: null q/k/v/o pointer");
   if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < 1)
     return fail(ATTN_EINVAL, "attn_fwd: sizes must be >= 1 (B=%d H=%d Hkv=%d Nq=%d Nk=%d)", B, H,
@@ -127,6 +127,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   if (!(scale > 0.f) || !(scale < 3.0e38f))
     return fail(ATTN_EINVAL, "attn_fwd: scale must be positive and finite");
   if (causal != 0 && causal != 1) return fail(ATTN_EINVAL, "attn_fwd: causal must be 0 or 1");
+  if (flags & ~unsigned(ATTN_FWD_EXP2_FMA)) return fail(ATTN_EINVAL, "attn_fwd: unknown flags 0x%x", flags);
   if (d != 64 && d != 128) return fail(ATTN_EUNSUPPORTED, "attn_fwd: head dim %d (need 64 or 128)", d);
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       (lse && !aligned(lse, 4)))
@@ -137,10 +138,17 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   if (st != ATTN_OK) return st;
   const char* err = nullptr;
   cudaError_t e = attn::prefill_launch(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal,
+                                       (flags & ATTN_FWD_EXP2_FMA) != 0,
                                        reinterpret_cast<cudaStream_t>(stream), &err);
   if (err) return fail(ATTN_ECUDA, "attn_fwd: %s", err);
   if (e != cudaSuccess) return fail(ATTN_ECUDA, "attn_fwd launch: %s", cudaGetErrorString(e));
   return ATTN_OK;
+}
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                     attn_stream_t stream) {
+  return attn_fwd_ex(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, 0u, stream);
 }
 
 attn_status paged_prefill(const void* q, const void* k_cache, const void* v_cache,

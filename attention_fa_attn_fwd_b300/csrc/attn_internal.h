@@ -17,7 +17,7 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64
 int prefill_smem_bytes(int d);
 cudaError_t prefill_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                            int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
-                           cudaStream_t stream, const char** err);
+                           bool poly_exp, cudaStream_t stream, const char** err);
 cudaError_t paged_prefill_launch(const void* q, const void* k_cache, const void* v_cache,
                                  const int32_t* block_table, const int32_t* kv_lens, int B, int H,
                                  int Hkv, int Nq, int d, int num_blocks, int max_blocks,

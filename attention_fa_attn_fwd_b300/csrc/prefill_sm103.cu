@@ -49,6 +49,7 @@
 #include <cstdio>
 
 #include "attn_internal.h"
+#include "exp2_poly.h"
 #include "ptx.cuh"
 
 namespace attn {
@@ -117,7 +118,31 @@ struct Args {
 
 constexpr int kPageTokens = 16;  // PagedAttention block size
 
-template <int D, bool kPaged>
+// 2^x for a pair of values on the FMA and integer pipes, without the MUFU
+// unit: x = n + f with n = round(x) (adding 1.5 * 2^23 rounds to an integer in
+// the low mantissa bits), f in [-1/2, 1/2]; 2^f by the least-squares cubic of
+// exp2_poly.h (relative error < 8e-5); 2^n by adding n to the exponent field.
+// Exactly 0 below -126 (so -inf, the mask value, gives 0).
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+  constexpr float kMagic = 12582912.f;  // 1.5 * 2^23
+  x.x = fmaxf(x.x, -127.f);
+  x.y = fmaxf(x.y, -127.f);
+  const float2 j = __fadd2_rn(x, make_float2(kMagic, kMagic));
+  const float2 n = __fadd2_rn(j, make_float2(-kMagic, -kMagic));
+  const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), x);
+  float2 p = __ffma2_rn(make_float2(kExp2Poly3, kExp2Poly3), f,
+                        make_float2(kExp2Poly2, kExp2Poly2));
+  p = __ffma2_rn(p, f, make_float2(kExp2Poly1, kExp2Poly1));
+  p = __ffma2_rn(p, f, make_float2(kExp2Poly0, kExp2Poly0));
+  float rx = __int_as_float(__float_as_int(p.x) + (__float_as_int(j.x) << 23));
+  float ry = __int_as_float(__float_as_int(p.y) + (__float_as_int(j.y) << 23));
+  return make_float2(x.x < -126.f ? 0.f : rx, x.y < -126.f ? 0.f : ry);
+}
+
+// kPolyExp: the exponentials of columns 64..127 of every score tile use
+// exp2_fma2 instead of the MUFU ex2, moving half of that work to the FMA pipe
+// (an opt-in variant; the MUFU path is the default).
+template <int D, bool kPaged, bool kPolyExp>
 __global__ void __launch_bounds__(384, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -467,8 +492,12 @@ __global__ void __launch_bounds__(384, 1)
           const int cc = half * 64 + 2 * e;
           float2 x = __ffma2_rn(make_float2(__uint_as_float(s[cc]), __uint_as_float(s[cc + 1])),
                                 c2, nm2);
-          x.x = ex2_approx(x.x);
-          x.y = ex2_approx(x.y);
+          if (kPolyExp && half == 1) {
+            x = exp2_fma2(x);
+          } else {
+            x.x = ex2_approx(x.x);
+            x.y = ex2_approx(x.y);
+          }
           acc[e & 3] = __fadd2_rn(acc[e & 3], x);
           pk[e] = pack_bf16x2(x.x, x.y);
         }
@@ -543,14 +572,14 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // Sets the kernel's dynamic shared memory limit once per device and variant.
-template <int D, bool kPaged>
+template <int D, bool kPaged, bool kPolyExp>
 cudaError_t configure_once() {
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(prefill_fwd_kernel<D, kPaged>,
+    e = cudaFuncSetAttribute(prefill_fwd_kernel<D, kPaged, kPolyExp>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
@@ -569,7 +598,7 @@ bool encode_q_o(CUtensorMap* tq, CUtensorMap* to, const void* q, void* o, int B,
          encode_tmap_bf16(to, o, 3, dq, sq, box, true, err);
 }
 
-template <int D>
+template <int D, bool kPolyExp>
 cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                    int Hkv, int Nq, int Nk, float scale, int causal, cudaStream_t stream,
                    const char** err) {
@@ -581,7 +610,7 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
   if (!encode_q_o<D>(&tq, &to, q, o, B, H, Nq, err)) return cudaErrorInvalidValue;
   if (!encode_tmap_bf16(&tk, k, 3, dk, sk, box, true, err)) return cudaErrorInvalidValue;
   if (!encode_tmap_bf16(&tv, v, 3, dk, sk, box, true, err)) return cudaErrorInvalidValue;
-  cudaError_t e = configure_once<D, false>();
+  cudaError_t e = configure_once<D, false, kPolyExp>();
   if (e != cudaSuccess) return e;
   Args a = {};
   a.lse = lse;
@@ -596,7 +625,8 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
   // K + V of every group at once above ~96 MB would thrash the 126 MB L2.
   a.group_major = (uint64_t(B) * Hkv * Nk * D * 4 > (96ull << 20)) ? 1 : 0;
   const unsigned grid = unsigned(a.n_pairs) * unsigned(B) * unsigned(H);
-  prefill_fwd_kernel<D, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
+  prefill_fwd_kernel<D, false, kPolyExp><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv,
+                                                                                     to, a);
   return cudaGetLastError();
 }
 
@@ -616,7 +646,7 @@ cudaError_t launch_paged(const void* q, const void* k_cache, const void* v_cache
   if (!encode_q_o<D>(&tq, &to, q, o, B, H, Nq, err)) return cudaErrorInvalidValue;
   if (!encode_tmap_bf16(&tk, k_cache, 3, dk, sk, box, true, err)) return cudaErrorInvalidValue;
   if (!encode_tmap_bf16(&tv, v_cache, 3, dk, sk, box, true, err)) return cudaErrorInvalidValue;
-  cudaError_t e = configure_once<D, true>();
+  cudaError_t e = configure_once<D, true, false>();
   if (e != cudaSuccess) return e;
   Args a = {};
   a.lse = lse;
@@ -635,7 +665,7 @@ cudaError_t launch_paged(const void* q, const void* k_cache, const void* v_cache
   a.oob_row = int(rows);
   a.group_major = 1;  // sequences have their own caches: keep one group's in L2
   const unsigned grid = unsigned(a.n_pairs) * unsigned(B) * unsigned(H);
-  prefill_fwd_kernel<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
+  prefill_fwd_kernel<D, true, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 
@@ -645,9 +675,15 @@ int prefill_smem_bytes(int d) { return d == 128 ? Cfg<128>::kSmemBytes : Cfg<64>
 
 cudaError_t prefill_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                            int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
-                           cudaStream_t stream, const char** err) {
-  if (d == 128) return launch<128>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, stream, err);
-  return launch<64>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, stream, err);
+                           bool poly_exp, cudaStream_t stream, const char** err) {
+  if (poly_exp) {
+    if (d == 128)
+      return launch<128, true>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, stream, err);
+    return launch<64, true>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, stream, err);
+  }
+  if (d == 128)
+    return launch<128, false>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, stream, err);
+  return launch<64, false>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, stream, err);
 }
 
 cudaError_t paged_prefill_launch(const void* q, const void* k_cache, const void* v_cache,

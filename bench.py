@@ -355,6 +355,25 @@ def run_ours(args, ws, rank, local):
     small_bytes = (dq.numel() * 2 * 2 + bt.numel() * 4 + sl.numel() * 4 + dlse.numel() * 4)
     dec_gbs = ws * (uniq_bytes + small_bytes) / (d_mean * 1e-3) / 1e9
 
+    # ---- the opt-in FMA-pipe exp2 variant of the prefill kernel (beside the step)
+    def prefill_fma():
+        binding.attn_fwd(q, k, v, causal=True, o=o, lse=lse, stream=stream, exp2_fma=True)
+
+    for _ in range(3):
+        flush()
+        prefill_fma()
+    Kx = max(3, min(K, 50))
+    x_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kx)]
+    for i in range(Kx):
+        flush()
+        x_evs[i][0].record(stream)
+        prefill_fma()
+        x_evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert binding.device_status(stream) == 0
+    px_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in x_evs), ws)
+    px_tflops = flops / (px_ms * 1e-3) / 1e12
+
     # ---- chunked prefill over the paged cache (reported beside the step)
     ppc = workloads.PAGED_PREFILL_WORKLOADS[PAGED_PREFILL]
     pp = workloads.paged_prefill_inputs(**ppc, seed=rank)
@@ -541,6 +560,9 @@ def run_ours(args, ws, rank, local):
                             "unit": "GB/s", "frac": k_gbs / peaks["hbm_gbs"],
                             "traffic": committed_traffic("decode_split_kernel", ["decode_sm103.cu", "ptx.cuh"]),
                             "kernel": "decode_split_kernel<128> + decode_merge_kernel<128>"},
+        "prefill_exp2_fma": {"ms": px_ms, "tflops": px_tflops, "frac_burst": px_tflops / ws / peak_tf,
+                             "note": "attn_fwd_ex(ATTN_FWD_EXP2_FMA): half the exponentials "
+                                     "on the FMA pipe"},
         "paged_prefill": {"workload": PAGED_PREFILL, "config": ppc, "ms": pp_ms,
                           "tflops": pp_tflops, "frac_burst": pp_tflops / ws / peak_tf,
                           "flops": pp_flops / ws, "kernel": "prefill_fwd_kernel<128, paged>",

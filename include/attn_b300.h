@@ -81,6 +81,26 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                      attn_stream_t stream);
 
 /*
+ * attn_fwd_ex -- attn_fwd with option flags (0 gives exactly attn_fwd).
+ *
+ *   ATTN_FWD_EXP2_FMA  half of the exponentials (columns 64..127 of every
+ *       128-key tile) are computed on the FMA and integer pipes instead of the
+ *       MUFU unit: 2^x = 2^round(x) * p(f) with a cubic p fitted by least
+ *       squares (relative error < 8e-5; see csrc/fit_exp2_poly.py).  The FSA
+ *       page ("FlashAttention systolic array" article, sections 2.1-2.3)
+ *       replaces the exponential unit by a least-squares piecewise-linear
+ *       exp2 to relieve the softmax bottleneck; this is the same idea on the
+ *       GPU's FMA pipe.  Results differ from the default path by rounding
+ *       only and stay within the same tolerances against the exact
+ *       definition.
+ * Unknown flag bits give ATTN_EINVAL.  Everything else as attn_fwd.
+ */
+#define ATTN_FWD_EXP2_FMA 1u
+ATTN_API attn_status attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
+                                 int causal, unsigned flags, attn_stream_t stream);
+
+/*
  * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs (the
  * per-row fp32 D = rowsum(dO o O), B*H*Nq floats rounded up to 256 bytes).
  * Returns 0 for invalid sizes.  Pure host function.

@@ -27,7 +27,7 @@ def lib():
 
 
 def test_header_declares_expected_api():
-    assert declared_functions() == sorted(["attn_fwd", "paged_decode", "paged_decode_workspace_size",
+    assert declared_functions() == sorted(["attn_fwd", "attn_fwd_ex", "paged_decode", "paged_decode_workspace_size",
                                            "paged_decode_noalloc", "paged_prefill", "attn_bwd",
                                            "attn_bwd_workspace_size", "kv_append",
                                            "kv_append_workspace_size", "attn_last_error",

@@ -130,3 +130,46 @@ def test_device_status_clean():
     q, k, v = (t.cuda() for t in _inputs(1, 2, 2, 256, 256, 64))
     binding.attn_fwd(q, k, v, causal=True)
     assert binding.device_status() == 0
+
+
+# ---- attn_fwd_ex with ATTN_FWD_EXP2_FMA (half of the exponentials on the FMA pipe)
+
+def _run_fma(q, k, v, causal, scale=None):
+    from attention_fa_attn_fwd_b300 import attn_fwd
+    o, lse = attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale, exp2_fma=True)
+    torch.cuda.synchronize()
+    return o.cpu(), lse.cpu()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [17, 200, 383])
+def test_exp2_fma_variant_ragged(d, causal, N):
+    q, k, v = _inputs(1, 4, 2, N, N, d, seed=N + 7)
+    o, lse = _run_fma(q, k, v, causal)
+    O, L = oracle.attention_ref(f64(q), f64(k), f64(v), 1 / math.sqrt(d), causal)
+    compare(f64(o), f64(lse), O, L, f"exp2-fma N={N} d={d} causal={causal}")
+
+
+def test_exp2_fma_variant_masked_rows_and_peaky():
+    q, k, v = _inputs(1, 2, 2, 300, 100, 128, seed=31)
+    o, lse = _run_fma(q, k, v, True)
+    assert torch.all(o[:, :, :200].float() == 0) and torch.all(torch.isneginf(lse[:, :, :200]))
+    q, k, v = _inputs(1, 2, 2, 512, 512, 128, seed=32, gain=3.0)
+    o, lse = _run_fma(q, k, v, True)
+    O, L = oracle.attention_ref(f64(q), f64(k), f64(v), 1 / math.sqrt(128), True)
+    compare(f64(o), f64(lse), O, L, "exp2-fma gain 3")
+
+
+def test_exp2_fma_variant_workload_sampled_and_differs_from_default():
+    cfg = workloads.PREFILL_WORKLOADS["gqa_b1h32kv8_n16384_d128_causal"]
+    q, k, v = workloads.prefill_inputs(**cfg)
+    o, lse = _run_fma(q, k, v, True)
+    rows = sample_rows(cfg["Nq"], 256, seed=5)
+    O, L = oracle.attention_ref(f64(q), f64(k), f64(v), 1 / math.sqrt(128), True, rows=rows)
+    compare(f64(o[:, :, rows]), f64(lse[:, :, rows]), O, L, "exp2-fma gqa n16384")
+    o2, _ = run_prefill(q[:, :, :512].contiguous(), k[:, :, :512].contiguous(),
+                        v[:, :, :512].contiguous(), True)
+    o3, _ = _run_fma(q[:, :, :512].contiguous(), k[:, :, :512].contiguous(),
+                     v[:, :, :512].contiguous(), True)
+    assert not torch.equal(o2, o3)  # the flag really switches the exponential
