@@ -10,6 +10,10 @@ N16384 d128; 335 MB on the device, larger than L2).  ``decode``: paged_decode
 on the 64-sequence workload (2.3 GB pool).  ``step``: both, as one bench step.
 ``paged_prefill``: chunked prefill of 8 x 2048 tokens over a paged cache.
 ``backward``: attn_bwd on the prefill workload (after one untimed attn_fwd).
+``sweep``: attn_fwd over the sequence-length sweep at B*N = 16384 tokens
+(N 512..16384, d 64/128, causal and not); prints TFLOP/s per configuration.
+``decode_sweep``: paged_decode of 64 sequences (32 at 16384) of one fixed
+context length (512..16384 tokens, H32 Hkv8 d128); prints KV GB/s per length.
 An L2 flush (``measure.L2Flush``: torch kernels, not this library's)
 precedes every kernel, as in bench.py.  Prints the CUDA-event time of each launch.
 """
@@ -25,9 +29,27 @@ from . import binding, workloads
 from .measure import L2Flush
 
 
+def _time(fn, flush, iters: int) -> float:
+    """Mean CUDA-event time (ms) of fn over iters runs after 2 warm-ups, each
+    run preceded by an L2 flush outside the events."""
+    for _ in range(2):
+        flush()
+        fn()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    for a, b in evs:
+        flush()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / iters
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=["prefill", "decode", "step", "paged_prefill", "backward"], default="step")
+    ap.add_argument("--case", choices=["prefill", "decode", "step", "paged_prefill", "backward", "sweep",
+                             "decode_sweep"], default="step")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--prefill", default="gqa_b1h32kv8_n16384_d128_causal")
     ap.add_argument("--decode-seqs", type=int, default=64,
@@ -75,6 +97,35 @@ def main(argv=None):
                           device=dev)
         runs.append(("attn_bwd", lambda: binding.attn_bwd(q, k, v, o, do, lse, causal=cfg["causal"],
                                                           dq=dq, dk=dk, dv=dv, workspace=bws)))
+    if args.case == "sweep":
+        for name, cfg in workloads.sweep_workloads().items():
+            q, k, v = (t.to(dev) for t in workloads.prefill_inputs(**cfg))
+            o = torch.empty_like(q)
+            lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+            ms = _time(lambda: binding.attn_fwd(q, k, v, causal=cfg["causal"], o=o, lse=lse),
+                       flush, args.iters)
+            fl = 4.0 * cfg["B"] * cfg["H"] * cfg["Nq"] * cfg["Nk"] * cfg["d"]
+            fl = fl / 2 if cfg["causal"] else fl
+            print(f"{name}: {ms:.4f} ms  {fl / ms / 1e9:.1f} TFLOP/s", flush=True)
+            del q, k, v, o, lse
+        return
+    if args.case == "decode_sweep":
+        for L in (512, 1024, 2048, 4096, 8192, 16384):
+            S = min(64, 64 * 8192 // L)
+            pb = workloads.paged_decode_inputs(num_seqs=S, H=32, Hkv=8, d=128, min_len=L,
+                                               max_len=L, group=1, shared_tokens=0, seed=0)
+            dq, kc, vc = pb.q.to(dev), pb.k_cache.to(dev), pb.v_cache.to(dev)
+            bt, sl = pb.block_table.to(dev), pb.seq_lens.to(dev)
+            do = torch.empty_like(dq)
+            dl = torch.empty(dq.shape[:2], dtype=torch.float32, device=dev)
+            n = binding.paged_decode_workspace_size(S, 32, 8, 128, bt.shape[1])
+            ws = torch.empty(n, dtype=torch.uint8, device=dev)
+            ms = _time(lambda: binding.paged_decode(dq, kc, vc, bt, sl, o=do, lse=dl, workspace=ws),
+                       flush, args.iters)
+            nbytes = pb.unique_valid_tokens() * 8 * 128 * 2 * 2
+            print(f"decode_s{S}_len{L}: {ms * 1e3:.1f} us  {nbytes / ms / 1e6:.1f} GB/s", flush=True)
+            del dq, kc, vc, bt, sl, do, dl, ws
+        return
     for it in range(args.iters):
         for name, fn in runs:
             flush()

@@ -34,6 +34,11 @@ GRAD_MAX_REL = 2e-2
 GRAD_FLOOR = 1e-2
 
 
+# (label, statistics) of every comparison made in this process; printed at the
+# end of a pytest run by conftest.py (and written to $PARITY_STATS_OUT if set).
+RECORDED = []
+
+
 def f64(t: torch.Tensor) -> np.ndarray:
     """Exact bf16 -> float64 through the oracle's own decoder."""
     t = t.detach().cpu().contiguous()
@@ -67,6 +72,7 @@ def compare(o_gpu: np.ndarray, lse_gpu, O_ref: np.ndarray, L_ref, what: str = ""
         lse_err = float(np.max(np.abs(lse_gpu[fin] - L_ref[fin]))) if fin.any() else 0.0
         stats["lse_max_abs"] = lse_err
         assert lse_err <= LSE_MAX_ABS, f"{what}: lse max abs {lse_err}"
+    RECORDED.append((what, stats))
     assert max_abs <= O_MAX_ABS, f"{what}: O max abs {max_abs} ({stats})"
     assert rel_rms <= O_REL_RMS, f"{what}: O rel rms {rel_rms} ({stats})"
     return stats
@@ -102,6 +108,7 @@ def compare_grad(g: np.ndarray, g_ref: np.ndarray, what: str = ""):
     floor = GRAD_FLOOR * np.sqrt(g_ref.size)
     rel_rms = float(np.sqrt(np.sum(diff ** 2)) / max(den, floor))
     stats = {"max_abs": max_abs, "ref_max": ref_max, "rel_rms": rel_rms}
+    RECORDED.append((what, stats))
     assert rel_rms <= GRAD_REL_RMS, f"{what}: rel rms {rel_rms} ({stats})"
     assert max_abs <= GRAD_MAX_REL * max(ref_max, GRAD_FLOOR), f"{what}: max abs {max_abs} ({stats})"
     return stats
