@@ -12,6 +12,9 @@ on the 64-sequence workload (2.3 GB pool).  ``step``: both, as one bench step.
 ``backward``: attn_bwd on the prefill workload (after one untimed attn_fwd).
 ``sweep``: attn_fwd over the sequence-length sweep at B*N = 16384 tokens
 (N 512..16384, d 64/128, causal and not); prints TFLOP/s per configuration.
+``configs``: attn_fwd on each named prefill workload (tiny, B2 H16 N2048,
+long-context GQA), with and without the FMA exp2, and the d64 sweep points
+with the FMA exp2; prints TFLOP/s.
 ``decode_sweep``: paged_decode of 64 sequences (32 at 16384) of one fixed
 context length (512..16384 tokens, H32 Hkv8 d128); prints KV GB/s per length.
 An L2 flush (``measure.L2Flush``: torch kernels, not this library's)
@@ -49,7 +52,7 @@ def _time(fn, flush, iters: int) -> float:
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", choices=["prefill", "decode", "step", "paged_prefill", "backward", "sweep",
-                             "decode_sweep"], default="step")
+                             "decode_sweep", "configs"], default="step")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--prefill", default="gqa_b1h32kv8_n16384_d128_causal")
     ap.add_argument("--decode-seqs", type=int, default=64,
@@ -97,6 +100,22 @@ def main(argv=None):
                           device=dev)
         runs.append(("attn_bwd", lambda: binding.attn_bwd(q, k, v, o, do, lse, causal=cfg["causal"],
                                                           dq=dq, dk=dk, dv=dv, workspace=bws)))
+    if args.case == "configs":
+        todo = [(n, c, False) for n, c in workloads.PREFILL_WORKLOADS.items()]
+        todo += [(n, c, True) for n, c in workloads.PREFILL_WORKLOADS.items()]
+        todo += [(n, c, True) for n, c in workloads.sweep_workloads().items() if c["d"] == 64]
+        for name, cfg, fma in todo:
+            q, k, v = (t.to(dev) for t in workloads.prefill_inputs(**cfg))
+            o = torch.empty_like(q)
+            lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+            ms = _time(lambda: binding.attn_fwd(q, k, v, causal=cfg["causal"], o=o, lse=lse,
+                                                exp2_fma=fma), flush, args.iters)
+            fl = 4.0 * cfg["B"] * cfg["H"] * cfg["Nq"] * cfg["Nk"] * cfg["d"]
+            fl = fl / 2 if cfg["causal"] else fl
+            tag = " exp2_fma" if fma else ""
+            print(f"{name}{tag}: {ms:.4f} ms  {fl / ms / 1e9:.1f} TFLOP/s", flush=True)
+            del q, k, v, o, lse
+        return
     if args.case == "sweep":
         for name, cfg in workloads.sweep_workloads().items():
             q, k, v = (t.to(dev) for t in workloads.prefill_inputs(**cfg))

@@ -151,3 +151,25 @@ def test_caller_workspace_and_determinism():
     with pytest.raises(binding.AttnError):
         binding.paged_decode(pb.q.cuda(), pb.k_cache.cuda(), pb.v_cache.cuda(),
                              pb.block_table.cuda(), pb.seq_lens.cuda(), workspace=ws[:16])
+
+
+def test_full_block_table_and_exact_block_boundaries():
+    # lengths that fill the table exactly, end on a block boundary, or one past it
+    # every sequence holds 704 tokens = 44 blocks, the whole table row
+    pb = workloads.paged_decode_inputs(**{**SMALL, "min_len": 704, "max_len": 704}, seed=8)
+    lens = pb.seq_lens.clone()
+    full = 16 * pb.max_blocks_per_seq
+    assert full == 704 and int(lens[0]) == full
+    lens[1] = full - 16
+    lens[2] = full - 15
+    lens[3] = 16 * 20 + 1
+    ids_ok = all(len(pb.logical_ids[s]) * 16 >= int(lens[s]) for s in range(4))
+    assert ids_ok
+    pb2 = workloads.PagedBatch(q=pb.q, k_cache=pb.k_cache, v_cache=pb.v_cache,
+                               block_table=pb.block_table, seq_lens=lens, block_size=16,
+                               logical_ids=pb.logical_ids, perm=pb.perm, k_unique=pb.k_unique,
+                               v_unique=pb.v_unique, num_unique=pb.num_unique)
+    o, lse = _gpu(pb2)
+    O, L = _ref(pb2, 1 / math.sqrt(128))
+    compare(f64(o), f64(lse), O, L, "full table / block boundaries")
+    assert binding.device_status() == binding.ATTN_OK
