@@ -343,16 +343,24 @@ __global__ void __launch_bounds__(384, 1)
       reg_fence<64>(s);
       reg_fence<64>(p);
       const int lim = row_last - j * 128 - wg * 64;  // columns > lim are masked
+      const bool masked = lim < 63;                   // only tiles on the diagonal or the tail
+      const float2 c2 = make_float2(c, c), nl2 = make_float2(neg_lse2, neg_lse2);
+      const float2 nd2 = make_float2(-drow, -drow);
       uint32_t pk[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        float x0 = ex2_approx(fmaf(__uint_as_float(s[2 * e]), c, neg_lse2));
-        float x1 = ex2_approx(fmaf(__uint_as_float(s[2 * e + 1]), c, neg_lse2));
-        if (2 * e > lim) x0 = 0.f;
-        if (2 * e + 1 > lim) x1 = 0.f;
-        const float d0 = x0 * (__uint_as_float(p[2 * e]) - drow);
-        const float d1 = x1 * (__uint_as_float(p[2 * e + 1]) - drow);
-        pk[e] = pack_bf16x2(d0, d1);
+        float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])),
+                              c2, nl2);
+        x.x = ex2_approx(x.x);
+        x.y = ex2_approx(x.y);
+        if (masked) {
+          if (2 * e > lim) x.x = 0.f;
+          if (2 * e + 1 > lim) x.y = 0.f;
+        }
+        const float2 dp = __fadd2_rn(make_float2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])),
+                                     nd2);
+        const float2 d = __fmul2_rn(x, dp);
+        pk[e] = pack_bf16x2(d.x, d.y);
       }
       tmem_st32(lane_base + wg * 128, pk);
       tmem_st_wait();
@@ -646,16 +654,27 @@ __global__ void __launch_bounds__(384, 1)
       // causally, if kj > query + off, i.e. q < kj - off - r0 - wg*64.
       const int lo = a.causal ? (kj - off - r0 - wg * 64) : -1;
       const bool key_ok = kj < a.Nk;
+      const bool masked = !key_ok || lo > 0;  // only tiles on the diagonal or the key tail
+      const float2 c2 = make_float2(c, c);
+      const float2* nl2 = reinterpret_cast<const float2*>(nl);
+      const float2* dd2 = reinterpret_cast<const float2*>(dd);
       uint32_t pp[32], pd[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        float x0 = ex2_approx(fmaf(__uint_as_float(s[2 * e]), c, nl[2 * e]));
-        float x1 = ex2_approx(fmaf(__uint_as_float(s[2 * e + 1]), c, nl[2 * e + 1]));
-        if (!key_ok || 2 * e < lo) x0 = 0.f;
-        if (!key_ok || 2 * e + 1 < lo) x1 = 0.f;
-        pp[e] = pack_bf16x2(x0, x1);
-        pd[e] = pack_bf16x2(x0 * (__uint_as_float(p[2 * e]) - dd[2 * e]),
-                            x1 * (__uint_as_float(p[2 * e + 1]) - dd[2 * e + 1]));
+        float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])),
+                              c2, nl2[e]);
+        x.x = ex2_approx(x.x);
+        x.y = ex2_approx(x.y);
+        if (masked) {
+          if (!key_ok || 2 * e < lo) x.x = 0.f;
+          if (!key_ok || 2 * e + 1 < lo) x.y = 0.f;
+        }
+        pp[e] = pack_bf16x2(x.x, x.y);
+        const float2 ndd = dd2[e];
+        const float2 dp = __fadd2_rn(make_float2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])),
+                                     make_float2(-ndd.x, -ndd.y));
+        const float2 d = __fmul2_rn(x, dp);
+        pd[e] = pack_bf16x2(d.x, d.y);
       }
       tmem_st32(lane_base + wg * 128, pp);
       tmem_st32(lane_base + wg * 128 + 64, pd);
