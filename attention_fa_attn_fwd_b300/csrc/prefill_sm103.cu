@@ -86,8 +86,9 @@ struct Cfg {
   static constexpr int kBarVF = kBarKE + kKStages;    // V stage full
   static constexpr int kBarVE = kBarVF + kVStages;    // V stage free
   static constexpr int kBarSF = kBarVE + kVStages;    // 2: S_i ready in TMEM
-  static constexpr int kBarPF = kBarSF + 2;           // 2: P_i written (and O_i rescaled)
-  static constexpr int kBarOF = kBarPF + 2;           // 2: last PV of tile i done
+  static constexpr int kBarPF = kBarSF + 2;           // 2: P_i keys 0..63 written (O_i rescaled)
+  static constexpr int kBarPF2 = kBarPF + 2;          // 2: P_i keys 64..127 written
+  static constexpr int kBarOF = kBarPF2 + 2;          // 2: last PV of tile i done
   static constexpr int kBarDrain = kBarOF + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) {
       uint32_t count = 1;
-      if (i == C::kBarPF || i == C::kBarPF + 1) count = 128;
+      if (i >= C::kBarPF && i < C::kBarPF2 + 2) count = 128;
       mbar_init(bar(i), count);
     }
     *abort_flag = 0;
@@ -348,7 +349,9 @@ __global__ void __launch_bounds__(384, 1)
             tail_r1 = min(128, nblk * kPageTokens - tail_tile * 128);
           }
         }
-        // O_i += P_i V_j, P_i read from the first 64 TMEM columns of S_i.
+        // O_i += P_i V_j, P_i read from the first 64 TMEM columns of S_i.  The
+        // products over keys 0..63 start as soon as that half of P is
+        // written, while the softmax warpgroup still works on keys 64..127.
         auto issue_pv = [&](int i, int j) -> bool {
           const int vs = j % C::kVStages;
           if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF + i), j & 1, abort_flag, err,
@@ -378,6 +381,12 @@ __global__ void __launch_bounds__(384, 1)
           const uint64_t vo = uint64_t((vs * C::kTileBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
+            if (kk == 4) {
+              if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF2 + i), j & 1, abort_flag, err,
+                                                     kErrTimeoutMma)))
+                return false;  // the caller drains the first half's MMAs
+              tc_fence_after();
+            }
             // V tile is [128 keys][D] in 64-column slabs: B operand MN-major,
             // 16 keys per MMA = 2 swizzle atoms of 8 rows (SBO 1024), next
             // 64 output columns one slab further (LBO = slab size).
@@ -486,6 +495,13 @@ __global__ void __launch_bounds__(384, 1)
       for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
+        if (half == 1) {
+          // keys 0..63 of P are in TMEM (and O was rescaled before): let the
+          // MMA warp start on them
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(C::kBarPF + wg));
+        }
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
@@ -510,7 +526,7 @@ __global__ void __launch_bounds__(384, 1)
       l += t.x + t.y;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::kBarPF + wg));
+      mbar_arrive(bar(C::kBarPF2 + wg));
     }
 
     // ---------------------------------------------------------- epilogue
