@@ -14,7 +14,6 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64
                       const char** err);
 
 // ---- prefill (prefill_sm103.cu)
-int prefill_smem_bytes(int d);
 cudaError_t prefill_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                            int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
                            bool poly_exp, cudaStream_t stream, const char** err);

@@ -687,8 +687,6 @@ cudaError_t launch_paged(const void* q, const void* k_cache, const void* v_cache
 
 }  // namespace
 
-int prefill_smem_bytes(int d) { return d == 128 ? Cfg<128>::kSmemBytes : Cfg<64>::kSmemBytes; }
-
 cudaError_t prefill_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                            int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
                            bool poly_exp, cudaStream_t stream, const char** err) {

@@ -24,7 +24,6 @@ precedes every kernel, as in bench.py.  Prints the CUDA-event time of each launc
 from __future__ import annotations
 
 import argparse
-import math
 
 import torch
 

@@ -173,3 +173,10 @@ def test_exp2_fma_variant_workload_sampled_and_differs_from_default():
     o3, _ = _run_fma(q[:, :, :512].contiguous(), k[:, :, :512].contiguous(),
                      v[:, :, :512].contiguous(), True)
     assert not torch.equal(o2, o3)  # the flag really switches the exponential
+
+
+def test_long_context_64k_sampled():
+    # 65536 keys: 256 K/V tiles per row block, 512 Q tiles per head
+    q, k, v = _inputs(1, 4, 1, 65536, 65536, 128, seed=41)
+    rows = sample_rows(65536, 24, seed=6)
+    check_prefill(q, k, v, True, rows=rows, what="N=65536 causal")
