@@ -51,6 +51,7 @@ SIGNATURES = {
     "kv_append_workspace_size": (_sz, [_i, _i]),
     "kv_append": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                        _vp, _sz, _vp]),
+    "attn_selftest_wait_timeout": (_i, [ctypes.c_uint, _vp]),
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_device_status": (_i, [_vp]),
 }
@@ -370,6 +371,12 @@ def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
 
 def kv_append_workspace_size(num_seqs: int, num_blocks: int) -> int:
     return int(load_library().kv_append_workspace_size(num_seqs, num_blocks))
+
+
+def selftest_wait_timeout(limit_us: int = 20000, stream=None) -> int:
+    """Run the bounded-wait self-test (see ``attn_selftest_wait_timeout``);
+    returns the status code (ATTN_OK when the expired wait was reported)."""
+    return int(load_library().attn_selftest_wait_timeout(int(limit_us), _stream_handle(stream)))
 
 
 def device_status(stream=None) -> int:

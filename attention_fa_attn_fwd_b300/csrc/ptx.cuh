@@ -20,6 +20,7 @@ enum : int {
   kErrTimeoutMma = 0x102,
   kErrTimeoutSoftmax = 0x103,
   kErrTimeoutEpilogue = 0x104,
+  kErrTimeoutSelftest = 0x1FF,  // the deliberate wait of attn_selftest_wait_timeout
   kErrDecodeBadBlock = 0x201,
   kErrPagedBadBlock = 0x202,   // paged prefill: block id outside [0, num_blocks)
   kErrPagedBadLength = 0x203,  // paged prefill: kv_lens[b] < 0 or > 16 * max_blocks
@@ -68,21 +69,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Returns false (without completing) if `abort_flag` is raised by another
 // thread, or after kWaitTimeoutNs, in which case it raises the flag itself and
 // records `code` in *err.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err, int code) {
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity,
+                                                volatile int* abort_flag, int* err, int code,
+                                                uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 15u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         if (err) atomicCAS(err, 0, code);
         return false;
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err, int code) {
+  return mbar_wait_limit(bar, parity, abort_flag, err, code, kWaitTimeoutNs);
 }
 
 // Drain wait used on the abort path: ignores the abort flag, gives up at the

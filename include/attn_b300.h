@@ -296,6 +296,20 @@ ATTN_API attn_status kv_append(const void* k_new, const void* v_new, void* k_cac
                                int block_size, void* workspace, size_t workspace_bytes,
                                attn_stream_t stream);
 
+/*
+ * attn_selftest_wait_timeout -- diagnostic for the library's failure
+ * detection (the source pages have no counterpart).  Every wait inside the
+ * kernels is bounded: if the data it waits for never arrives, it gives up,
+ * records an error code read by attn_device_status() and lets the kernel
+ * return, so a broken pipeline never hangs the GPU.  This call launches one
+ * warp that waits on a barrier nothing will ever signal, with a limit of
+ * limit_us microseconds (1 .. 1e6), synchronises `stream` and checks that the
+ * expiry was detected and reported.  Returns ATTN_OK if it was, ATTN_EDEVICE
+ * if not, ATTN_EINVAL for a bad limit, ATTN_ECUDA if a CUDA call failed.
+ * It does not touch the error words attn_device_status() reads.
+ */
+ATTN_API attn_status attn_selftest_wait_timeout(unsigned limit_us, attn_stream_t stream);
+
 /* Message for the last non-OK status returned on the calling thread. */
 ATTN_API const char* attn_last_error(void);
 

@@ -30,7 +30,8 @@ def test_header_declares_expected_api():
     assert declared_functions() == sorted(["attn_fwd", "attn_fwd_ex", "paged_decode", "paged_decode_workspace_size",
                                            "paged_decode_noalloc", "paged_prefill", "attn_bwd",
                                            "attn_bwd_workspace_size", "kv_append",
-                                           "kv_append_workspace_size", "attn_last_error",
+                                           "kv_append_workspace_size", "attn_selftest_wait_timeout",
+                                           "attn_last_error",
                                            "attn_device_status"])
 
 
@@ -200,3 +201,8 @@ def _app(lib, **kw):
 def test_kv_append_rejects_bad_arguments(lib, kw, status):
     assert _app(lib, **kw) == status
     assert lib.attn_last_error()
+
+
+def test_selftest_rejects_bad_limit(lib):
+    assert lib.attn_selftest_wait_timeout(0, None) == binding.ATTN_EINVAL
+    assert lib.attn_selftest_wait_timeout(2_000_000, None) == binding.ATTN_EINVAL
