@@ -17,7 +17,7 @@ Sources (page title, then the part of the page):
   computation builds the full N x N matrix; FlashAttention-2 reaches the same
   result incrementally (online softmax) without storing it.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent (the same readings hold for the kernels):
 
 * ``scale`` is an argument; the definition's value is 1/sqrt(d).
 * Causal masking is bottom-right aligned: query row i (0-based) may attend key

@@ -9,7 +9,7 @@ and 3.0.7 (block size 16; parallel sampling shares prefix blocks); section
 3.0.2 item 3 (sharing must leave every sequence's attention unchanged).
 
 The pages name copy-on-write but do not spell it out; the plain reading used
-here (and stated in DESIGN.md):
+here (the one the kernels implement):
 
 * A sequence's LOGICAL cache is the list of its tokens' K/V rows.  Appending T
   tokens extends that list; nothing else changes -- in particular, appending
