@@ -272,13 +272,21 @@ def paged_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
     _need(block_table, "block_table", torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)
     S, H, d = q.shape
-    num_blocks, Hkv, block_size, _ = k_cache.shape
+    num_blocks, Hkv, block_size, dk = k_cache.shape
+    if v_cache.shape != k_cache.shape or dk != d:
+        raise ValueError("k_cache / v_cache / q shapes disagree")
+    if block_table.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_table / seq_lens must have num_seqs rows")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if o is None:
         o = torch.empty_like(q)
+    else:
+        _need(o, "o", torch.bfloat16, 3)
     if lse is None:
         lse = torch.empty((S, H), dtype=torch.float32, device=q.device)
+    else:
+        _need(lse, "lse", torch.float32, 2)
     st = lib.paged_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                   block_table.data_ptr(), seq_lens.data_ptr(), S, H, Hkv, d,
                                   num_blocks, block_table.shape[1], block_size, float(scale),
