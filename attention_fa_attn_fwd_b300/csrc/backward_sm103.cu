@@ -19,7 +19,8 @@
 //                      dQ += dS K accumulated in TMEM.
 //   bwd_dkdv_kernel    KV-stationary: a CTA owns 128 keys of one KV head and
 //                      streams, for every query head of its group, the Q/dO
-//                      tiles that attend them: S^T = K Q^T and dP^T = V dO^T,
+//                      tiles that attend them (in half-tiles of 64 queries,
+//                      each released as soon as its products are issued): S^T = K Q^T and dP^T = V dO^T,
 //                      P^T and dS^T (bf16) back into TMEM, dV += P^T dO and
 //                      dK += dS^T Q accumulated in TMEM.
 // Splitting dQ from dK/dV recomputes S and dP once more (7 instead of 5
@@ -412,17 +413,21 @@ __global__ void __launch_bounds__(384, 1)
 template <int D>
 struct DkvCfg : BCfg<D> {
   using B_ = BCfg<D>;
-  static constexpr int kQStages = (D == 128) ? 2 : 3;  // (Q, dO, -lse2, D) per stage
+  // Q and dO stream through half-stages of 64 queries each (one half of a
+  // 128-query tile), so a half is released as soon as its products are done.
+  static constexpr int kHalfSlabBytes = 64 * 128;                   // 64 rows x 128 B
+  static constexpr int kHalfBytes = B_::kSlabs * kHalfSlabBytes;    // 64 rows of Q (or dO)
+  static constexpr int kHS = (D == 128) ? 4 : 6;                    // half-stages
   static constexpr int kOffK = 0;
   static constexpr int kOffV = B_::kTileBytes;
-  static constexpr int kOffQ = 2 * B_::kTileBytes;                       // Q stages
-  static constexpr int kOffDO = kOffQ + kQStages * B_::kTileBytes;       // dO stages
-  static constexpr int kOffStat = kOffDO + kQStages * B_::kTileBytes;    // [stage][2][128] fp32
-  static constexpr int kOffBar = kOffStat + kQStages * 2 * 128 * 4;
+  static constexpr int kOffQ = 2 * B_::kTileBytes;                  // Q half-stages
+  static constexpr int kOffDO = kOffQ + kHS * kHalfBytes;           // dO half-stages
+  static constexpr int kOffStat = kOffDO + kHS * kHalfBytes;        // [hs][2][64] fp32
+  static constexpr int kOffBar = kOffStat + kHS * 2 * 64 * 4;
   static constexpr int kBarKVF = 0;
-  static constexpr int kBarQF = 1;
-  static constexpr int kBarQE = kBarQF + kQStages;
-  static constexpr int kBarSF = kBarQE + kQStages;  // 2: S^T_h and dP^T_h in TMEM
+  static constexpr int kBarQF = 1;                  // kHS: half-stage full (32 arrivals + tx)
+  static constexpr int kBarQE = kBarQF + kHS;       // kHS: half-stage free
+  static constexpr int kBarSF = kBarQE + kHS;       // 2: S^T_h and dP^T_h in TMEM
   static constexpr int kBarPF = kBarSF + 2;         // 2: P^T_h, dS^T_h written (128 each)
   static constexpr int kBarOF = kBarPF + 2;         // dK, dV complete
   static constexpr int kBarDrain = kBarOF + 1;
@@ -431,6 +436,7 @@ struct DkvCfg : BCfg<D> {
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   // half h: S^T_h at h*128 (64 columns), dP^T_h at h*128 + 64; dV, dK after.
   static constexpr uint32_t kColDV = 256, kColDK = 256 + D;
+  static_assert(kHS * kHalfBytes >= B_::kTileBytes, "epilogue staging needs one tile");
 };
 
 template <int D>
@@ -474,7 +480,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < C::kNumBars; ++i) {
       uint32_t cnt = 1;
       if (i == C::kBarPF || i == C::kBarPF + 1) cnt = 128;
-      if (i >= C::kBarQF && i < C::kBarQF + C::kQStages) cnt = 32;
+      if (i >= C::kBarQF && i < C::kBarQF + C::kHS) cnt = 32;
       mbar_init(bar(i), cnt);
     }
     *abort_flag = 0;
@@ -510,18 +516,20 @@ __global__ void __launch_bounds__(384, 1)
       }
       bool ok = true;
       int issued = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int st = it % C::kQStages;
+      // Half u = 2*it + h: queries h*64 .. h*64+63 of (query head, tile) it.
+      for (int u = 0; u < 2 * n_it; ++u) {
+        const int it = u >> 1, h = u & 1;
+        const int hs = u % C::kHS;
         const int hq = b * a.H + g * G + it / per_head;  // query (b, h) row of the tensor maps
-        const int r0 = (qt0 + it % per_head) * 128;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarQE + st), ((it / C::kQStages) & 1) ^ 1,
+        const int r0 = (qt0 + it % per_head) * 128 + h * 64;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarQE + hs), ((u / C::kHS) & 1) ^ 1,
                                                abort_flag, err, kErrTimeoutProducer));
         if (!ok) break;
-        // Row statistics of the 128 queries: -lse*log2(e) (-inf past Nq) and D.
-        float* sp = stat + st * 256;
+        // Row statistics of the 64 queries: -lse*log2(e) (-inf past Nq) and D.
+        float* sp = stat + hs * 128;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int cidx = lane * 4 + e;
+        for (int e = 0; e < 2; ++e) {
+          const int cidx = lane * 2 + e;
           const int r = r0 + cidx;
           float nl = -INFINITY, dd = 0.f;
           if (r < a.Nq) {
@@ -529,26 +537,26 @@ __global__ void __launch_bounds__(384, 1)
             dd = a.delta[size_t(hq) * a.Nq + r];
           }
           sp[cidx] = nl;
-          sp[128 + cidx] = dd;
+          sp[64 + cidx] = dd;
         }
         if (lane == 0)
-          mbar_arrive_expect_tx(bar(C::kBarQF + st), 2 * C::kTileBytes);
+          mbar_arrive_expect_tx(bar(C::kBarQF + hs), 2 * C::kHalfBytes);
         else
-          mbar_arrive(bar(C::kBarQF + st));
+          mbar_arrive(bar(C::kBarQF + hs));
         __syncwarp();
         for (int s = 0; s < C::kSlabs; ++s) {
-          tma_load_3d_elect(sbase + C::kOffQ + st * C::kTileBytes + s * C::kSlabBytes, &tm_q,
-                            bar(C::kBarQF + st), s * 64, r0, hq);
-          tma_load_3d_elect(sbase + C::kOffDO + st * C::kTileBytes + s * C::kSlabBytes, &tm_do,
-                            bar(C::kBarQF + st), s * 64, r0, hq);
+          tma_load_3d_elect(sbase + C::kOffQ + hs * C::kHalfBytes + s * C::kHalfSlabBytes, &tm_q,
+                            bar(C::kBarQF + hs), s * 64, r0, hq);
+          tma_load_3d_elect(sbase + C::kOffDO + hs * C::kHalfBytes + s * C::kHalfSlabBytes, &tm_do,
+                            bar(C::kBarQF + hs), s * 64, r0, hq);
         }
-        issued = it + 1;
+        issued = u + 1;
       }
       if (!ok) {
         const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
         mbar_wait_drain(bar(C::kBarKVF), 0, deadline);
-        for (int it = max(0, issued - C::kQStages); it < issued; ++it)
-          mbar_wait_drain(bar(C::kBarQF + it % C::kQStages), (it / C::kQStages) & 1, deadline);
+        for (int u = max(0, issued - C::kHS); u < issued; ++u)
+          mbar_wait_drain(bar(C::kBarQF + u % C::kHS), (u / C::kHS) & 1, deadline);
       }
     } else if (warp == 1 && n_it > 0) {
       // ------------------------------------------------------ MMA issuer
@@ -558,61 +566,61 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t v_desc = smem_desc_sw128(sbase + C::kOffV, 16, 1024);
       const uint64_t q_desc = smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
       const uint64_t do_desc = smem_desc_sw128(sbase + C::kOffDO, 16, 1024);
-      const uint64_t qmn_desc = smem_desc_sw128(sbase + C::kOffQ, C::kSlabBytes, 1024);
-      const uint64_t domn_desc = smem_desc_sw128(sbase + C::kOffDO, C::kSlabBytes, 1024);
-      // S^T_h = K Q[h]^T, dP^T_h = V dO[h]^T over queries h*64 .. h*64+63.
-      auto issue_s_dp = [&](int h, int st) {
-        const uint64_t so = uint64_t((st * C::kTileBytes + h * 8192) >> 4);
+      const uint64_t qmn_desc = smem_desc_sw128(sbase + C::kOffQ, C::kHalfSlabBytes, 1024);
+      const uint64_t domn_desc = smem_desc_sw128(sbase + C::kOffDO, C::kHalfSlabBytes, 1024);
+      // S^T_h = K Q[h]^T, dP^T_h = V dO[h]^T over the 64 queries of half u.
+      auto issue_s_dp = [&](int u) -> bool {
+        const int h = u & 1, hs = u % C::kHS;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarQF + hs), (u / C::kHS) & 1, abort_flag,
+                                               err, kErrTimeoutMma)))
+          return false;
+        tc_fence_after();
+        const uint64_t so = uint64_t((hs * C::kHalfBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t o16 = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tmem + h * 128, k_desc + o16, q_desc + so + o16, kIdescHalf,
+          const uint64_t ok_ = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
+          const uint64_t oq = uint64_t(((kk >> 2) * C::kHalfSlabBytes + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + h * 128, k_desc + ok_, q_desc + so + oq, kIdescHalf,
                       kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t o16 = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tmem + h * 128 + 64, v_desc + o16, do_desc + so + o16, kIdescHalf,
+          const uint64_t ok_ = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
+          const uint64_t oq = uint64_t(((kk >> 2) * C::kHalfSlabBytes + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + h * 128 + 64, v_desc + ok_, do_desc + so + oq, kIdescHalf,
                       kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBarSF + h));
+        return true;
       };
-      // dV += P^T_h dO[h], dK += dS^T_h Q[h] (16 queries per MMA).
-      auto issue_acc = [&](int h, int it) -> bool {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF + h), it & 1, abort_flag, err,
+      // dV += P^T_h dO[h], dK += dS^T_h Q[h] (16 queries per MMA); frees the half-stage.
+      auto issue_acc = [&](int u) -> bool {
+        const int h = u & 1, hs = u % C::kHS;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF + h), (u >> 1) & 1, abort_flag, err,
                                                kErrTimeoutMma)))
           return false;
         tc_fence_after();
-        const int st = it % C::kQStages;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t o16 = uint64_t((st * C::kTileBytes + (h * 64 + kk * 16) * 128) >> 4);
-          const uint32_t acc = (it > 0 || h > 0 || kk > 0) ? 1u : 0u;
+          const uint64_t o16 = uint64_t((hs * C::kHalfBytes + kk * 16 * 128) >> 4);
+          const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
           mma_bf16_ts(tmem + C::kColDV, tmem + h * 128 + kk * 8, domn_desc + o16, kIdescAcc, acc);
           mma_bf16_ts(tmem + C::kColDK, tmem + h * 128 + 64 + kk * 8, qmn_desc + o16, kIdescAcc,
                       acc);
         }
-        if (h == 1) mma_commit(bar(C::kBarQE + st));
+        mma_commit(bar(C::kBarQE + hs));
         return true;
       };
       bool ok = __all_sync(0xffffffffu,
                            mbar_wait(bar(C::kBarKVF), 0, abort_flag, err, kErrTimeoutMma));
-      // Issue order: S/dP(it,0) [acc(it-1,1)] S/dP(it,1) acc(it,0).
+      // Issue order per tile it: S/dP(it,0) [acc(it-1,1)] S/dP(it,1) acc(it,0).
       for (int it = 0; ok && it < n_it; ++it) {
-        const int st = it % C::kQStages;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarQF + st), (it / C::kQStages) & 1,
-                                               abort_flag, err, kErrTimeoutMma));
-        if (!ok) break;
-        tc_fence_after();
-        issue_s_dp(0, st);
-        if (it > 0) {
-          ok = issue_acc(1, it - 1);
-          if (!ok) break;
-        }
-        issue_s_dp(1, st);
-        ok = issue_acc(0, it);
+        ok = issue_s_dp(2 * it);
+        if (ok && it > 0) ok = issue_acc(2 * it - 1);
+        if (ok) ok = issue_s_dp(2 * it + 1);
+        if (ok) ok = issue_acc(2 * it);
       }
-      if (ok && n_it > 0) ok = issue_acc(1, n_it - 1);
+      if (ok && n_it > 0) ok = issue_acc(2 * n_it - 1);
       if (ok) {
         mma_commit(bar(C::kBarOF));
       } else {
@@ -631,9 +639,9 @@ __global__ void __launch_bounds__(384, 1)
     const float c = a.c_log2;
     bool ok = !dead;
     for (int it = 0; ok && it < n_it; ++it) {
-      const int st = it % C::kQStages;
+      const int u = 2 * it + wg, hs = u % C::kHS;
       const int r0 = (qt0 + it % per_head) * 128;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarQF + st), (it / C::kQStages) & 1,
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarQF + hs), (u / C::kHS) & 1,
                                              abort_flag, err, kErrTimeoutSoftmax));
       if (!ok) break;
       ok = __all_sync(0xffffffffu,
@@ -648,8 +656,8 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld_wait();
       reg_fence<64>(s);
       reg_fence<64>(p);
-      const float* nl = stat + st * 256 + wg * 64;
-      const float* dd = nl + 128;
+      const float* nl = stat + hs * 128;
+      const float* dd = nl + 64;
       // Column q (query r0 + wg*64 + q) is masked if this key is past Nk or,
       // causally, if kj > query + off, i.e. q < kj - off - r0 - wg*64.
       const int lo = a.causal ? (kj - off - r0 - wg * 64) : -1;
@@ -753,8 +761,11 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   const uint64_t sq[2] = {uint64_t(D) * 2, uint64_t(Nq) * D * 2};
   const uint64_t dk_[3] = {uint64_t(D), uint64_t(Nk), uint64_t(B) * Hkv};
   const uint64_t sk[2] = {uint64_t(D) * 2, uint64_t(Nk) * D * 2};
-  CUtensorMap tq, tdo, tk, tv, tdq, tdk, tdv;
-  if (!encode_tmap_bf16(&tq, q, 3, dq_, sq, box, true, err) ||
+  const uint32_t box64[3] = {64, 64, 1};
+  CUtensorMap tq, tdo, tk, tv, tdq, tdk, tdv, tq64, tdo64;
+  if (!encode_tmap_bf16(&tq64, q, 3, dq_, sq, box64, true, err) ||
+      !encode_tmap_bf16(&tdo64, dout, 3, dq_, sq, box64, true, err) ||
+      !encode_tmap_bf16(&tq, q, 3, dq_, sq, box, true, err) ||
       !encode_tmap_bf16(&tdo, dout, 3, dq_, sq, box, true, err) ||
       !encode_tmap_bf16(&tdq, dq, 3, dq_, sq, box, true, err) ||
       !encode_tmap_bf16(&tk, k, 3, dk_, sk, box, true, err) ||
@@ -791,8 +802,8 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid_kv = unsigned(B) * Hkv * unsigned((Nk + 127) / 128);
-  bwd_dkdv_kernel<D><<<grid_kv, 384, DkvCfg<D>::kSmemBytes, stream>>>(tq, tdo, tk, tv, tdk, tdv,
-                                                                       a);
+  bwd_dkdv_kernel<D><<<grid_kv, 384, DkvCfg<D>::kSmemBytes, stream>>>(tq64, tdo64, tk, tv, tdk,
+                                                                       tdv, a);
   return cudaGetLastError();
 }
 
