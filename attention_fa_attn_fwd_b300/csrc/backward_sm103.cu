@@ -84,6 +84,8 @@ __device__ __forceinline__ void stage_row32(uint8_t* tile, int row, int c0, cons
 }
 
 struct BArgs {
+  const uint16_t* q;     // [B*H, Nq, D] bf16 (the dQ kernel reads its rows directly)
+  const uint16_t* dout;  // [B*H, Nq, D] bf16
   const float* lse;  // [B, H, Nq] natural log, from the forward pass
   float* delta;      // [B, H, Nq] workspace: rowsum(dO o O)
   int B, H, Hkv, Nq, Nk;
@@ -129,14 +131,14 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restri
 template <int D>
 struct DqCfg : BCfg<D> {
   using B_ = BCfg<D>;
-  static constexpr int kKStages = (D == 128) ? 3 : 4;
-  static constexpr int kVStages = (D == 128) ? 2 : 3;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffDO = B_::kTileBytes;
-  static constexpr int kOffK = 2 * B_::kTileBytes;
+  // Q and dO live in TMEM (the A operand of S and dP), so shared memory holds
+  // only the K and V stages.
+  static constexpr int kKStages = (D == 128) ? 4 : 6;
+  static constexpr int kVStages = (D == 128) ? 3 : 5;
+  static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKStages * B_::kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * B_::kTileBytes;
-  static constexpr int kBarQF = 0;
+  static constexpr int kBarQF = 0;                  // Q, dO in TMEM (256 arrivals)
   static constexpr int kBarKF = 1;
   static constexpr int kBarKE = kBarKF + kKStages;
   static constexpr int kBarVF = kBarKE + kKStages;
@@ -148,14 +150,17 @@ struct DqCfg : BCfg<D> {
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-  // half h: S_h at h*128 (64 columns), dP_h at h*128 + 64; dQ at 256.
+  // half h: S_h at h*128 (64 columns), dP_h at h*128 + 64; dQ at 256;
+  // Q and dO as bf16 pairs (D/2 columns each) after it.
   static constexpr uint32_t kColDQ = 256;
+  static constexpr uint32_t kColQ = 256 + D;
+  static constexpr uint32_t kColDO = kColQ + D / 2;
+  static_assert(kColDO + D / 2 <= B_::kTmemCols, "TMEM budget");
 };
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_dq, const BArgs a) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -182,13 +187,12 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i)
-      mbar_init(bar(i), (i == C::kBarPF || i == C::kBarPF + 1) ? 128u : 1u);
+      mbar_init(bar(i), i == C::kBarQF ? 256u
+                        : (i == C::kBarPF || i == C::kBarPF + 1) ? 128u : 1u);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_do);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_dq);
@@ -208,12 +212,6 @@ __global__ void __launch_bounds__(384, 1)
       // ------------------------------------------------------ producer
       int k_issued = 0, v_issued = 0;
       bool ok = true;
-      mbar_arrive_expect_tx_elect(bar(C::kBarQF), 2 * C::kTileBytes);
-      for (int s = 0; s < C::kSlabs; ++s) {
-        tma_load_3d_elect(sbase + C::kOffQ + s * C::kSlabBytes, &tm_q, bar(C::kBarQF), s * 64, q0, bh);
-        tma_load_3d_elect(sbase + C::kOffDO + s * C::kSlabBytes, &tm_do, bar(C::kBarQF), s * 64, q0,
-                          bh);
-      }
       for (int j = 0; j < n; ++j) {
         const int ks = j % C::kKStages, vs = j % C::kVStages;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarKE + ks), ((j / C::kKStages) & 1) ^ 1,
@@ -235,7 +233,6 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) {
         const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
-        mbar_wait_drain(bar(C::kBarQF), 0, deadline);
         for (int j = max(0, k_issued - C::kKStages); j < k_issued; ++j)
           mbar_wait_drain(bar(C::kBarKF + j % C::kKStages), (j / C::kKStages) & 1, deadline);
         for (int j = max(0, v_issued - C::kVStages); j < v_issued; ++j)
@@ -245,27 +242,27 @@ __global__ void __launch_bounds__(384, 1)
       // ------------------------------------------------------ MMA issuer
       constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, 0);
       constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, 1);
-      const uint64_t q_desc = smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
-      const uint64_t do_desc = smem_desc_sw128(sbase + C::kOffDO, 16, 1024);
       const uint64_t k_desc = smem_desc_sw128(sbase + C::kOffK, 16, 1024);
       const uint64_t v_desc = smem_desc_sw128(sbase + C::kOffV, 16, 1024);
       const uint64_t kmn_desc = smem_desc_sw128(sbase + C::kOffK, C::kSlabBytes, 1024);
       // S_h = Q K_j[h]^T and dP_h = dO V_j[h]^T over keys h*64 .. h*64+63
-      // (64 rows further into the K / V tile: +8 KB per slab).
+      // (64 rows further into the K / V tile: +8 KB per slab).  A (Q, dO)
+      // comes from TMEM, 16 elements = 8 columns per MMA, so shared memory
+      // only supplies the 64-row B operand.
       auto issue_s_dp = [&](int h, int ks, int vs) {
         const uint64_t ko = uint64_t((ks * C::kTileBytes + h * 8192) >> 4);
         const uint64_t vo = uint64_t((vs * C::kTileBytes + h * 8192) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tmem + h * 128, q_desc + off, k_desc + ko + off, kIdescHalf,
+          mma_bf16_ts(tmem + h * 128, tmem + C::kColQ + kk * 8, k_desc + ko + off, kIdescHalf,
                       kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tmem + h * 128 + 64, do_desc + off, v_desc + vo + off, kIdescHalf,
-                      kk > 0 ? 1u : 0u);
+          mma_bf16_ts(tmem + h * 128 + 64, tmem + C::kColDO + kk * 8, v_desc + vo + off,
+                      kIdescHalf, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBarSF + h));
       };
@@ -328,6 +325,29 @@ __global__ void __launch_bounds__(384, 1)
       neg_lse2 = neg_lse2_of(a.lse[size_t(bh) * a.Nq + q_row]);
       drow = a.delta[size_t(bh) * a.Nq + q_row];
     }
+    if (n > 0) {
+      // This thread's row of Q (first warpgroup) or dO (second) into TMEM as
+      // bf16 pairs, the A operand of S and dP; rows past Nq are zero.
+      const uint16_t* src = wg == 0 ? a.q : a.dout;
+      const uint4* rp = reinterpret_cast<const uint4*>(src + (size_t(bh) * a.Nq + q_row) * D);
+      const uint32_t col = wg == 0 ? C::kColQ : C::kColDO;
+#pragma unroll
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        uint32_t w[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint4 x = q_row < a.Nq ? __ldg(rp + c0 / 4 + e) : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * e] = x.x;
+          w[4 * e + 1] = x.y;
+          w[4 * e + 2] = x.z;
+          w[4 * e + 3] = x.w;
+        }
+        tmem_st32(lane_base + col + c0, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarQF));
+    }
     const float c = a.c_log2;
     bool ok = !dead;
     for (int j = 0; ok && j < n; ++j) {
@@ -374,7 +394,7 @@ __global__ void __launch_bounds__(384, 1)
                       mbar_wait(bar(C::kBarOF), 0, abort_flag, err, kErrTimeoutEpilogue));
       tc_fence_after();
     }
-    uint8_t* stage = smem + C::kOffQ;  // Q is no longer read once dQ is complete
+    uint8_t* stage = smem + C::kOffK;  // every K/V stage is consumed once dQ is complete
     if (ok) {
 #pragma unroll
       for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
@@ -394,7 +414,7 @@ __global__ void __launch_bounds__(384, 1)
     named_bar_sync(1, 256);
     if (!*abort_flag && ok && warp == 4 && lane == 0) {
       for (int s = 0; s < C::kSlabs; ++s)
-        tma_store_3d(&tm_dq, sbase + C::kOffQ + s * C::kSlabBytes, s * 64, q0, bh);
+        tma_store_3d(&tm_dq, sbase + C::kOffK + s * C::kSlabBytes, s * 64, q0, bh);
       bulk_commit_group();
       bulk_wait_group_read0();
     }
@@ -762,11 +782,9 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   const uint64_t dk_[3] = {uint64_t(D), uint64_t(Nk), uint64_t(B) * Hkv};
   const uint64_t sk[2] = {uint64_t(D) * 2, uint64_t(Nk) * D * 2};
   const uint32_t box64[3] = {64, 64, 1};
-  CUtensorMap tq, tdo, tk, tv, tdq, tdk, tdv, tq64, tdo64;
+  CUtensorMap tk, tv, tdq, tdk, tdv, tq64, tdo64;
   if (!encode_tmap_bf16(&tq64, q, 3, dq_, sq, box64, true, err) ||
       !encode_tmap_bf16(&tdo64, dout, 3, dq_, sq, box64, true, err) ||
-      !encode_tmap_bf16(&tq, q, 3, dq_, sq, box, true, err) ||
-      !encode_tmap_bf16(&tdo, dout, 3, dq_, sq, box, true, err) ||
       !encode_tmap_bf16(&tdq, dq, 3, dq_, sq, box, true, err) ||
       !encode_tmap_bf16(&tk, k, 3, dk_, sk, box, true, err) ||
       !encode_tmap_bf16(&tv, v, 3, dk_, sk, box, true, err) ||
@@ -780,6 +798,8 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   if (e != cudaSuccess) return e;
 
   BArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.dout = static_cast<const uint16_t*>(dout);
   a.lse = lse;
   a.delta = delta;
   a.B = B;
@@ -798,7 +818,7 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid_dq = unsigned(B) * H * unsigned((Nq + 127) / 128);
-  bwd_dq_kernel<D><<<grid_dq, 384, DqCfg<D>::kSmemBytes, stream>>>(tq, tdo, tk, tv, tdq, a);
+  bwd_dq_kernel<D><<<grid_dq, 384, DqCfg<D>::kSmemBytes, stream>>>(tk, tv, tdq, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid_kv = unsigned(B) * Hkv * unsigned((Nk + 127) / 128);
