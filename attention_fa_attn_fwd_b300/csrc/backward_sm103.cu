@@ -64,6 +64,17 @@ struct BCfg {
 
 // ---------------------------------------------------------------- helpers
 
+// 32 lanes x 16 columns of 32-bit into tensor memory (one row per thread).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
 // 128-byte-swizzled row write of 32 fp32 values (scaled, rounded to bf16)
 // into a 128-row staging tile laid out in 64-column slabs.
 template <int D>
@@ -144,7 +155,7 @@ struct DqCfg : BCfg<D> {
   static constexpr int kBarVF = kBarKE + kKStages;
   static constexpr int kBarVE = kBarVF + kVStages;
   static constexpr int kBarSF = kBarVE + kVStages;  // 2: S_h and dP_h of half h in TMEM
-  static constexpr int kBarPF = kBarSF + 2;         // 2: dS_h written (128 arrivals each)
+  static constexpr int kBarPF = kBarSF + 2;         // 2: dS_h written (256 arrivals each)
   static constexpr int kBarOF = kBarPF + 2;         // dQ complete
   static constexpr int kBarDrain = kBarOF + 1;
   static constexpr int kNumBars = kBarDrain + 1;
@@ -187,8 +198,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i)
-      mbar_init(bar(i), i == C::kBarQF ? 256u
-                        : (i == C::kBarPF || i == C::kBarPF + 1) ? 128u : 1u);
+      mbar_init(bar(i), (i == C::kBarQF || i == C::kBarPF || i == C::kBarPF + 1) ? 256u : 1u);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -266,7 +276,8 @@ __global__ void __launch_bounds__(384, 1)
         }
         mma_commit(bar(C::kBarSF + h));
       };
-      // dQ += dS_h K_j[h]: A = dS_h (bf16 in TMEM), 16 keys per MMA.
+      // dQ += dS_h K_j[h]: A = dS_h (bf16 in TMEM), 16 keys per MMA; keys
+      // 0-31 of the half at columns 0-15 of its block, keys 32-63 at 32-47.
       auto issue_dq = [&](int h, int j) -> bool {
         if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF + h), j & 1, abort_flag, err,
                                                kErrTimeoutMma)))
@@ -275,7 +286,7 @@ __global__ void __launch_bounds__(384, 1)
         const int ks = j % C::kKStages;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ts(tmem + C::kColDQ, tmem + h * 128 + kk * 8,
+          mma_bf16_ts(tmem + C::kColDQ, tmem + h * 128 + (kk >> 1) * 32 + (kk & 1) * 8,
                       kmn_desc + uint64_t((ks * C::kTileBytes + (h * 64 + kk * 16) * 128) >> 4),
                       kIdescDQ, (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
         if (h == 1) mma_commit(bar(C::kBarKE + ks));
@@ -314,7 +325,7 @@ __global__ void __launch_bounds__(384, 1)
   } else {
     setmaxnreg_inc<C::kRegsHigh>();
     // -------------------------------------------------------- compute
-    const int wg = (warp >> 2) - 1;   // which 64-column half
+    const int wg = (warp >> 2) - 1;   // which 32 columns of each 64-column half
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
@@ -350,43 +361,47 @@ __global__ void __launch_bounds__(384, 1)
     }
     const float c = a.c_log2;
     bool ok = !dead;
+    const float2 c2 = make_float2(c, c), nl2 = make_float2(neg_lse2, neg_lse2);
+    const float2 nd2 = make_float2(-drow, -drow);
+    // Both warpgroups take every half: this one its columns wg*32 .. wg*32+31
+    // of S_h and dP_h, writing dS over the first 16 of them.
     for (int j = 0; ok && j < n; ++j) {
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(bar(C::kBarSF + wg), j & 1, abort_flag, err, kErrTimeoutSoftmax));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t s[64], p[64];
-      tmem_ld32(lane_base + wg * 128, s);
-      tmem_ld32(lane_base + wg * 128 + 32, s + 32);
-      tmem_ld32(lane_base + wg * 128 + 64, p);
-      tmem_ld32(lane_base + wg * 128 + 96, p + 32);
-      tmem_ld_wait();
-      reg_fence<64>(s);
-      reg_fence<64>(p);
-      const int lim = row_last - j * 128 - wg * 64;  // columns > lim are masked
-      const bool masked = lim < 63;                   // only tiles on the diagonal or the tail
-      const float2 c2 = make_float2(c, c), nl2 = make_float2(neg_lse2, neg_lse2);
-      const float2 nd2 = make_float2(-drow, -drow);
-      uint32_t pk[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])),
-                              c2, nl2);
-        x.x = ex2_approx(x.x);
-        x.y = ex2_approx(x.y);
-        if (masked) {
-          if (2 * e > lim) x.x = 0.f;
-          if (2 * e + 1 > lim) x.y = 0.f;
+      for (int h = 0; h < 2; ++h) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(C::kBarSF + h), j & 1, abort_flag, err, kErrTimeoutSoftmax));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t col = h * 128 + wg * 32;
+        uint32_t s[32], p[32];
+        tmem_ld32(lane_base + col, s);
+        tmem_ld32(lane_base + col + 64, p);
+        tmem_ld_wait();
+        reg_fence<32>(s);
+        reg_fence<32>(p);
+        const int lim = row_last - j * 128 - h * 64 - wg * 32;  // columns > lim are masked
+        const bool masked = lim < 31;  // only tiles on the diagonal or the tail
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float2 x = __ffma2_rn(
+              make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), c2, nl2);
+          x.x = ex2_approx(x.x);
+          x.y = ex2_approx(x.y);
+          if (masked) {
+            if (2 * e > lim) x.x = 0.f;
+            if (2 * e + 1 > lim) x.y = 0.f;
+          }
+          const float2 dp = __fadd2_rn(
+              make_float2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])), nd2);
+          const float2 d = __fmul2_rn(x, dp);
+          pk[e] = pack_bf16x2(d.x, d.y);
         }
-        const float2 dp = __fadd2_rn(make_float2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])),
-                                     nd2);
-        const float2 d = __fmul2_rn(x, dp);
-        pk[e] = pack_bf16x2(d.x, d.y);
+        tmem_st16(lane_base + col, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::kBarPF + h));
       }
-      tmem_st32(lane_base + wg * 128, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarPF + wg));
     }
     // -------------------------------------------------------- epilogue
     if (ok && n > 0) {
