@@ -318,22 +318,27 @@ __global__ void __launch_bounds__(384, 1)
         const uint64_t v_desc = smem_desc_sw128(sbase + C::kOffV, C::kSlabBytes, 1024);
         bool ok = true;
         // S_i = Q_i K_j^T.  The last Q tile using K_j frees its stage.
+        // Tile 1 skips the K-full wait when tile 0 has just waited for the
+        // same stage and phase: a wait costs this warp over 100 cycles even
+        // when the phase is complete, and the tensor pipe idles meanwhile.
         auto issue_qk = [&](int i, int j) -> bool {
           const int ks = j % C::kKStages;
           if (j == 0 && !__all_sync(0xffffffffu, mbar_wait(bar(C::kBarQF + i), 0, abort_flag, err,
                                                            kErrTimeoutMma)))
             return false;
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarKF + ks), (j / C::kKStages) & 1,
+          if (!(i == 1 && j < n_t[0]) &&
+              !__all_sync(0xffffffffu, mbar_wait(bar(C::kBarKF + ks), (j / C::kKStages) & 1,
                                                  abort_flag, err, kErrTimeoutMma)))
             return false;
           tc_fence_after();
           const uint32_t d_tmem = tmem + C::kColS + i * 128;
-          const uint64_t qo = uint64_t((i * C::kTileBytes) >> 4);
-          const uint64_t ko = uint64_t((ks * C::kTileBytes) >> 4);
+          const uint64_t qa = desc_add(q_desc, uint32_t((i * C::kTileBytes) >> 4));
+          const uint64_t kb = desc_add(k_desc, uint32_t((ks * C::kTileBytes) >> 4));
+          // 16 head dims (32 bytes, 2 address units) per MMA, four per 64-column slab.
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = uint64_t(((kk >> 2) * C::kSlabBytes + (kk & 3) * 32) >> 4);
-            mma_bf16_ss(d_tmem, q_desc + qo + off, k_desc + ko + off, kIdescQK, kk > 0 ? 1u : 0u);
+          for (int g = 0; g < D / 64; ++g) {
+            const uint32_t o = uint32_t((g * C::kSlabBytes) >> 4);
+            mma4_bf16_ss<2, 2>(d_tmem, desc_add(qa, o), desc_add(kb, o), kIdescQK, g > 0 ? 1u : 0u);
           }
           mma_commit(bar(C::kBarSF + i));
           if (i == 1 || j >= n_t[1]) mma_commit(bar(C::kBarKE + ks));
@@ -357,7 +362,8 @@ __global__ void __launch_bounds__(384, 1)
           if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF + i), j & 1, abort_flag, err,
                                                  kErrTimeoutMma)))
             return false;
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarVF + vs), (j / C::kVStages) & 1,
+          if (!(i == 1 && j < n_t[0]) &&
+              !__all_sync(0xffffffffu, mbar_wait(bar(C::kBarVF + vs), (j / C::kVStages) & 1,
                                                  abort_flag, err, kErrTimeoutMma)))
             return false;
           if constexpr (kPaged) {
@@ -378,22 +384,18 @@ __global__ void __launch_bounds__(384, 1)
           }
           tc_fence_after();
           const uint32_t a_tmem = tmem + C::kColS + i * 128;
-          const uint64_t vo = uint64_t((vs * C::kTileBytes) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            if (kk == 4) {
-              if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF2 + i), j & 1, abort_flag, err,
-                                                     kErrTimeoutMma)))
-                return false;  // the caller drains the first half's MMAs
-              tc_fence_after();
-            }
-            // V tile is [128 keys][D] in 64-column slabs: B operand MN-major,
-            // 16 keys per MMA = 2 swizzle atoms of 8 rows (SBO 1024), next
-            // 64 output columns one slab further (LBO = slab size).
-            mma_bf16_ts(tmem + C::kColO + i * D, a_tmem + kk * 8,
-                        v_desc + vo + uint64_t((kk * 2048) >> 4), kIdescPV,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-          }
+          const uint32_t d_tmem = tmem + C::kColO + i * D;
+          // V tile is [128 keys][D] in 64-column slabs: B operand MN-major,
+          // 16 keys per MMA = 2 swizzle atoms of 8 rows (SBO 1024, 2048 bytes
+          // = 128 address units per MMA), next 64 output columns one slab
+          // further (LBO = slab size).  P: 16 keys = 8 TMEM columns per MMA.
+          const uint64_t vb = desc_add(v_desc, uint32_t((vs * C::kTileBytes) >> 4));
+          mma4_bf16_ts<8, 128>(d_tmem, a_tmem, vb, kIdescPV, j > 0 ? 1u : 0u);
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF2 + i), j & 1, abort_flag, err,
+                                                 kErrTimeoutMma)))
+            return false;  // the caller drains the first half's MMAs
+          tc_fence_after();
+          mma4_bf16_ts<8, 128>(d_tmem, a_tmem + 32, desc_add(vb, 512), kIdescPV, 1u);
           if (i == 1 || j >= n_t[1]) mma_commit(bar(C::kBarVE + vs));
           if (j == n_t[i] - 1) mma_commit(bar(C::kBarOF + i));
           return true;
