@@ -38,6 +38,9 @@ SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, ctypes.c_uint,
                          _vp]),
+    "attn_fwd_host_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "attn_fwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _i,
+                           _vp]),
     "paged_decode_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "paged_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                           _vp, _vp, _vp, _sz, _vp]),
@@ -152,6 +155,74 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                           lse.data_ptr() if lse is not None else None,
                           B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
                           _stream_handle(stream))
+    _check(st)
+    return o, lse
+
+
+def _need_host(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def attn_fwd_host_workspace_size(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:
+    return int(load_library().attn_fwd_host_workspace_size(B, H, Hkv, Nq, Nk, d))
+
+
+def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                  causal: bool = False, scale: Optional[float] = None,
+                  o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                  want_lse: bool = True, workspace: Optional[torch.Tensor] = None,
+                  chunks: int = 0, device=None,
+                  stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """``attn_fwd_host``: the forward on HOST tensors (pinned for overlap).
+
+    q [B,H,Nq,d], k/v [B,Hkv,Nk,d] bf16 CPU tensors; o / lse are CPU outputs
+    (allocated pinned if not given).  ``workspace`` is a uint8 CUDA tensor of
+    at least ``attn_fwd_host_workspace_size`` bytes (allocated on ``device``,
+    default the current one, if not given).  Asynchronous on ``stream``: the
+    outputs are valid once the stream has reached this call's end.
+    """
+    lib = load_library()
+    _need_host(q, "q", torch.bfloat16, 4)
+    _need_host(k, "k", torch.bfloat16, 4)
+    _need_host(v, "v", torch.bfloat16, 4)
+    B, H, Nq, d = q.shape
+    _, Hkv, Nk, _ = k.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    else:
+        _need_host(o, "o", torch.bfloat16, 4)
+        if o.shape != q.shape:
+            raise ValueError("o must have q's shape")
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+    elif lse is not None:
+        _need_host(lse, "lse", torch.float32, 3)
+        if tuple(lse.shape) != (B, H, Nq):
+            raise ValueError("lse must be [B, H, Nq]")
+    need = int(lib.attn_fwd_host_workspace_size(B, H, Hkv, Nq, Nk, d))
+    if workspace is None:
+        dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    elif not workspace.is_cuda or workspace.dtype != torch.uint8:
+        raise TypeError("workspace must be a uint8 CUDA tensor")
+    st = lib.attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr() if lse is not None else None,
+                           B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                           workspace.data_ptr(), workspace.numel(), int(chunks),
+                           _stream_handle(stream))
     _check(st)
     return o, lse
 

@@ -151,6 +151,50 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   return attn_fwd_ex(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, 0u, stream);
 }
 
+size_t attn_fwd_host_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d) {
+  if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || H % Hkv != 0 || (d != 64 && d != 128))
+    return 0;
+  return attn::fwd_host_workspace_bytes(B, H, Hkv, Nq, Nk, d);
+}
+
+attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                          int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                          void* workspace, size_t workspace_bytes, int chunks,
+                          attn_stream_t stream) {
+  if (!q || !k || !v || !o || !workspace)
+    return fail(ATTN_EINVAL, "attn_fwd_host: null q/k/v/o/workspace pointer");
+  if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < 1)
+    return fail(ATTN_EINVAL, "attn_fwd_host: sizes must be >= 1 (B=%d H=%d Hkv=%d Nq=%d Nk=%d)",
+                B, H, Hkv, Nq, Nk);
+  if (H % Hkv != 0)
+    return fail(ATTN_EINVAL, "attn_fwd_host: H=%d is not a multiple of Hkv=%d", H, Hkv);
+  if (!(scale > 0.f) || !(scale < 3.0e38f))
+    return fail(ATTN_EINVAL, "attn_fwd_host: scale must be positive and finite");
+  if (causal != 0 && causal != 1) return fail(ATTN_EINVAL, "attn_fwd_host: causal must be 0 or 1");
+  if (d != 64 && d != 128)
+    return fail(ATTN_EUNSUPPORTED, "attn_fwd_host: head dim %d (need 64 or 128)", d);
+  if (chunks < 0 || chunks > attn::fwd_host_max_chunks())
+    return fail(ATTN_EINVAL, "attn_fwd_host: chunks=%d (0 = automatic, else 1..%d)", chunks,
+                attn::fwd_host_max_chunks());
+  if (!aligned(workspace, 256))
+    return fail(ATTN_EINVAL, "attn_fwd_host: workspace must be 256-byte aligned");
+  const long long ctas = (long long)B * H * ((Nq + 127) / 128);
+  if (ctas >= (1LL << 31)) return fail(ATTN_EINVAL, "attn_fwd_host: problem too large");
+  const size_t need = attn::fwd_host_workspace_bytes(B, H, Hkv, Nq, Nk, d);
+  if (workspace_bytes < need)
+    return fail(ATTN_EINVAL, "attn_fwd_host: workspace of %zu bytes, need %zu", workspace_bytes,
+                need);
+  attn_status st = check_device();
+  if (st != ATTN_OK) return st;
+  const char* err = nullptr;
+  cudaError_t e = attn::fwd_host_launch(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal,
+                                        workspace, chunks, reinterpret_cast<cudaStream_t>(stream),
+                                        &err);
+  if (err) return fail(ATTN_ECUDA, "attn_fwd_host: %s", err);
+  if (e != cudaSuccess) return fail(ATTN_ECUDA, "attn_fwd_host: %s", cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
 attn_status paged_prefill(const void* q, const void* k_cache, const void* v_cache,
                           const int32_t* block_table, const int32_t* seq_lens, int num_seqs, int H,
                           int Hkv, int Nq, int d, int num_blocks, int max_blocks_per_seq,

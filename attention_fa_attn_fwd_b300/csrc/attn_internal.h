@@ -24,6 +24,14 @@ cudaError_t paged_prefill_launch(const void* q, const void* k_cache, const void*
                                  cudaStream_t stream, const char** err);
 int prefill_take_device_error();  // reads and clears (synchronous)
 
+// ---- forward from host buffers, copies overlapped (host_pipeline.cu)
+size_t fwd_host_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d);
+int fwd_host_max_chunks();
+cudaError_t fwd_host_launch(const void* q_h, const void* k_h, const void* v_h, void* o_h,
+                            float* lse_h, int B, int H, int Hkv, int Nq, int Nk, int d,
+                            float scale, int causal, void* workspace, int chunks,
+                            cudaStream_t stream, const char** err);
+
 // ---- paged decode (decode_sm103.cu)
 struct DecodePlan {
   int blocks_per_split;

@@ -7,7 +7,8 @@
  * ---------------------------------------
  * - Pointers to tensors are DEVICE pointers on the current CUDA device,
  *   allocated and owned by the caller; the library never frees or retains
- *   them.  The library allocates no device memory in these calls.
+ *   them (attn_fwd_host takes host tensors and a device workspace, see
+ *   there).  The library allocates no device memory in these calls.
  * - Element types: q, k, v, o, k_cache, v_cache are bfloat16 (passed as
  *   void*), lse is float32, block_table and seq_lens are int32.
  * - Every tensor is dense and contiguous in the layout stated per call.
@@ -99,6 +100,44 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
 ATTN_API attn_status attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                                  int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
                                  int causal, unsigned flags, attn_stream_t stream);
+
+/*
+ * attn_fwd_host_workspace_size -- bytes of device workspace attn_fwd_host
+ * needs: Q, K, V, O and LSE of the whole problem, each rounded up to 256
+ * bytes.  Returns 0 for invalid sizes.  Pure host function.
+ */
+ATTN_API size_t attn_fwd_host_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d);
+
+/*
+ * attn_fwd_host -- attn_fwd on HOST buffers, the transfers overlapped with
+ * the computation (the same operation and results as attn_fwd, bit for bit).
+ *
+ *   q, k, v  HOST pointers, layouts as attn_fwd (read).
+ *   o, lse   HOST pointers, layouts as attn_fwd (written); lse may be NULL.
+ *   workspace        DEVICE buffer of at least attn_fwd_host_workspace_size()
+ *                    bytes, 256-byte aligned, owned by the caller.
+ *   chunks  0 = automatic (8), else 1..16: the (batch, KV head) units are
+ *           split into this many contiguous ranges (at most one per unit);
+ *           range c+1 is copied to the device while range c computes and
+ *           range c-1's results are copied back.
+ *
+ * Host buffers should be page-locked (cudaHostAlloc / pinned): then the call
+ * returns without waiting and the copies overlap the kernels.  Pageable
+ * buffers give the same results but the runtime may block the calling thread
+ * during the copies.  The call is stream-ordered: the input copies start
+ * after the work already queued on `stream`, and work queued on `stream`
+ * after this call starts only after o and lse have reached host memory.  The
+ * host buffers must stay valid until then.  The library creates two copy
+ * streams and a few events per calling thread and device on the first call
+ * and keeps them; it allocates no device memory.
+ *
+ * Requirements as attn_fwd (except host pointers need no alignment), plus a
+ * large enough, aligned workspace (else ATTN_EINVAL).
+ */
+ATTN_API attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int B, int H, int Hkv, int Nq, int Nk, int d,
+                                   float scale, int causal, void* workspace,
+                                   size_t workspace_bytes, int chunks, attn_stream_t stream);
 
 /*
  * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs (the

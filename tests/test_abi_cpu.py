@@ -27,7 +27,9 @@ def lib():
 
 
 def test_header_declares_expected_api():
-    assert declared_functions() == sorted(["attn_fwd", "attn_fwd_ex", "paged_decode", "paged_decode_workspace_size",
+    assert declared_functions() == sorted(["attn_fwd", "attn_fwd_ex", "attn_fwd_host",
+                                           "attn_fwd_host_workspace_size",
+                                           "paged_decode", "paged_decode_workspace_size",
                                            "paged_decode_noalloc", "paged_prefill", "attn_bwd",
                                            "attn_bwd_workspace_size", "kv_append",
                                            "kv_append_workspace_size", "attn_selftest_wait_timeout",
@@ -215,3 +217,43 @@ def test_attn_fwd_ex_flags(lib):
                          0.125, 0, 0x2, None)
     assert st == binding.ATTN_EINVAL
     assert b"flags" in lib.attn_last_error()
+
+
+def _fwd_host(lib, **kw):
+    a = dict(q=_fake(1), k=_fake(2), v=_fake(3), o=_fake(4), lse=None, B=1, H=4, Hkv=2, Nq=128,
+             Nk=256, d=128, scale=0.088, causal=1, ws=_fake(5), wsb=1 << 30, chunks=0,
+             stream=None)
+    a.update(kw)
+    return lib.attn_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Hkv"],
+                             a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"], a["ws"], a["wsb"],
+                             a["chunks"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), binding.ATTN_EINVAL),
+    (dict(ws=None), binding.ATTN_EINVAL),
+    (dict(ws=ctypes.c_void_p(0x10010)), binding.ATTN_EINVAL),   # not 256-byte aligned
+    (dict(wsb=1024), binding.ATTN_EINVAL),                       # too small
+    (dict(chunks=-1), binding.ATTN_EINVAL),
+    (dict(chunks=17), binding.ATTN_EINVAL),
+    (dict(H=3), binding.ATTN_EINVAL),
+    (dict(Nq=0), binding.ATTN_EINVAL),
+    (dict(causal=2), binding.ATTN_EINVAL),
+    (dict(scale=float("nan")), binding.ATTN_EINVAL),
+    (dict(d=80), binding.ATTN_EUNSUPPORTED),
+])
+def test_attn_fwd_host_rejects_bad_arguments(lib, kw, status):
+    assert _fwd_host(lib, **kw) == status
+    assert lib.attn_last_error()
+
+
+def test_fwd_host_workspace_size(lib):
+    # Q + K + V + O + LSE, each rounded up to 256 bytes
+    B, H, Hkv, Nq, Nk, d = 2, 8, 2, 300, 500, 64
+    r = lambda n: (n + 255) // 256 * 256
+    want = (r(B * H * Nq * d * 2) + 2 * r(B * Hkv * Nk * d * 2) + r(B * H * Nq * d * 2)
+            + r(B * H * Nq * 4))
+    assert lib.attn_fwd_host_workspace_size(B, H, Hkv, Nq, Nk, d) == want
+    assert lib.attn_fwd_host_workspace_size(B, 7, Hkv, Nq, Nk, d) == 0
+    assert lib.attn_fwd_host_workspace_size(B, H, Hkv, Nq, Nk, 96) == 0
+    assert lib.attn_fwd_host_workspace_size(0, H, Hkv, Nq, Nk, d) == 0
