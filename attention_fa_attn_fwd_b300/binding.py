@@ -188,7 +188,10 @@ def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     (allocated pinned if not given).  ``workspace`` is a uint8 CUDA tensor of
     at least ``attn_fwd_host_workspace_size`` bytes (allocated on ``device``,
     default the current one, if not given).  Asynchronous on ``stream``: the
-    outputs are valid once the stream has reached this call's end.
+    outputs are valid once the stream has reached this call's end, and every
+    host tensor passed in must stay alive and unchanged until then (a
+    temporary such as ``q.pin_memory()`` may be freed and its pinned block
+    reused before the copies run).
     """
     lib = load_library()
     _need_host(q, "q", torch.bfloat16, 4)

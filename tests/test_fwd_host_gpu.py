@@ -70,10 +70,12 @@ def test_stream_ordered_back_to_back_calls_share_a_workspace():
     ws = torch.empty(binding.attn_fwd_host_workspace_size(B, H, Hkv, N, N, d), dtype=torch.uint8,
                      device="cuda")
     side = torch.cuda.Stream()
+    # The host tensors must outlive the asynchronous calls: keep the pinned
+    # copies referenced until the stream has finished.
+    pinned = [tuple(t.pin_memory() for t in x) for x in ins]
     outs = []
-    for q, k, v in ins:
-        outs.append(binding.attn_fwd_host(q.pin_memory(), k.pin_memory(), v.pin_memory(),
-                                          workspace=ws, chunks=4, stream=side))
+    for q, k, v in pinned:
+        outs.append(binding.attn_fwd_host(q, k, v, workspace=ws, chunks=4, stream=side))
     side.synchronize()
     for (o, lse), (o_ref, lse_ref) in zip(outs, refs):
         assert torch.equal(_bits(o), _bits(o_ref))
