@@ -129,7 +129,10 @@ ATTN_API size_t attn_fwd_host_workspace_size(int B, int H, int Hkv, int Nq, int 
  * after this call starts only after o and lse have reached host memory.  The
  * host buffers must stay valid until then.  The library creates two copy
  * streams and a few events per calling thread and device on the first call
- * and keeps them; it allocates no device memory.
+ * and keeps them; it allocates no device memory.  The call can be captured
+ * into a CUDA graph (the copy streams fork from and join back to `stream`;
+ * make one call outside capture first so the copy streams exist, and use
+ * pinned buffers).
  *
  * Requirements as attn_fwd (except host pointers need no alignment), plus a
  * large enough, aligned workspace (else ATTN_EINVAL).

@@ -88,3 +88,31 @@ def test_workspace_too_small_is_rejected():
     with pytest.raises(binding.AttnError) as e:
         binding.attn_fwd_host(q, k, v, workspace=ws)
     assert e.value.status == binding.ATTN_EINVAL
+
+
+def test_captured_in_a_cuda_graph_and_replayed():
+    # The copy streams fork from and join back to the capturing stream, so the
+    # whole call (copies in, kernels, copies out) becomes one graph.
+    B, H, Hkv, N, d = 1, 8, 2, 512, 128
+    q, k, v = workloads.prefill_inputs(B, H, Hkv, N, N, d, seed=31)
+    o_ref, lse_ref = _device_reference(q, k, v, True)
+    qp, kp, vp = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    ws = torch.empty(binding.attn_fwd_host_workspace_size(B, H, Hkv, N, N, d), dtype=torch.uint8,
+                     device="cuda")
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        binding.attn_fwd_host(qp, kp, vp, causal=True, o=o, lse=lse, workspace=ws, chunks=2,
+                              stream=side)  # first call creates the copy streams
+    side.synchronize()
+    o.zero_()
+    lse.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        binding.attn_fwd_host(qp, kp, vp, causal=True, o=o, lse=lse, workspace=ws, chunks=2,
+                              stream=side)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(o), _bits(o_ref))
+    assert torch.equal(_bits(lse), _bits(lse_ref))
