@@ -174,6 +174,33 @@ __global__ void __launch_bounds__(384, 1)
     const int grp = blockIdx.x / per_group, r = blockIdx.x % per_group;
     pair = r / G;
     bh = grp * G + r % G;
+    if constexpr (kPaged) {
+      // Sequences have their own lengths: take the groups of the longest
+      // sequences first (ties by index), so the longest ones do not run
+      // last.  Group grp is KV head grp % Hkv of the (grp / Hkv)-th longest
+      // sequence; each warp ranks the lengths itself (up to 64 sequences,
+      // else index order).
+      if (a.B <= 64) {
+        const int k = grp / a.Hkv;
+        const int L0 = lane < a.B ? a.kv_lens[lane] : 0;
+        const int L1 = lane + 32 < a.B ? a.kv_lens[lane + 32] : 0;
+        int mine = -1;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int c = lane + 32 * t;
+          const int Lc = t == 0 ? L0 : L1;
+          int rank = 0;
+          for (int o = 0; o < a.B; ++o) {
+            const int Lo = __shfl_sync(0xffffffffu, o < 32 ? L0 : L1, o & 31);
+            rank += (Lo > Lc || (Lo == Lc && o < c)) ? 1 : 0;
+          }
+          if (c < a.B && rank == k) mine = c;
+        }
+        const unsigned found = __ballot_sync(0xffffffffu, mine >= 0);
+        const int seq = __shfl_sync(0xffffffffu, mine, __ffs(int(found)) - 1);
+        bh = seq * a.H + (grp % a.Hkv) * G + r % G;
+      }
+    }
   } else {
     bh = blockIdx.x % BH;
     pair = blockIdx.x / BH;
