@@ -132,3 +132,17 @@ def test_paged_prefill_workload_sampled():
     O, L = _ref(pb, True, rows=rows)
     compare(f64(o[:, :, rows]), f64(lse[:, :, rows]), O, L, "paged prefill workload")
     assert binding.device_status() == binding.ATTN_OK
+
+
+@pytest.mark.parametrize("num_seqs,min_hist,max_hist", [
+    (64, 0, 300),    # longest-first order, two candidates per lane when ranking
+    (6, 120, 120),   # equal lengths: the ranking breaks ties by sequence index
+    (70, 0, 90),     # more than 64 sequences: plain index order
+])
+def test_grid_order_by_sequence_length(num_seqs, min_hist, max_hist):
+    pb = _small(num_seqs=num_seqs, H=4, Hkv=2, d=64, Nq=33, min_hist=min_hist,
+                max_hist=max_hist, seed=num_seqs)
+    o, lse = _gpu(pb, True)
+    O, L = _ref(pb, True)
+    compare(f64(o), f64(lse), O, L, f"paged prefill {num_seqs} seqs, hist {min_hist}..{max_hist}")
+    assert binding.device_status() == binding.ATTN_OK
