@@ -220,33 +220,32 @@ __global__ void __launch_bounds__(384, 1)
     setmaxnreg_dec<C::kRegsLow>();
     if (warp == 0 && n > 0) {
       // ------------------------------------------------------ producer
-      int k_issued = 0, v_issued = 0;
+      // K_j and V_j complete on one barrier (K-full of K_j's stage, expecting
+      // both tiles' bytes), so the MMA warp waits once per tile: every wait
+      // costs that warp over 100 cycles even on a completed phase.
+      int issued = 0;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
         const int ks = j % C::kKStages, vs = j % C::kVStages;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarKE + ks), ((j / C::kKStages) & 1) ^ 1,
                                                abort_flag, err, kErrTimeoutProducer));
         if (!ok) break;
-        mbar_arrive_expect_tx_elect(bar(C::kBarKF + ks), C::kTileBytes);
-        for (int s = 0; s < C::kSlabs; ++s)
-          tma_load_3d_elect(sbase + C::kOffK + ks * C::kTileBytes + s * C::kSlabBytes, &tm_k,
-                            bar(C::kBarKF + ks), s * 64, j * 128, zkv);
-        k_issued = j + 1;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarVE + vs), ((j / C::kVStages) & 1) ^ 1,
                                                abort_flag, err, kErrTimeoutProducer));
         if (!ok) break;
-        mbar_arrive_expect_tx_elect(bar(C::kBarVF + vs), C::kTileBytes);
+        mbar_arrive_expect_tx_elect(bar(C::kBarKF + ks), 2 * C::kTileBytes);
+        for (int s = 0; s < C::kSlabs; ++s)
+          tma_load_3d_elect(sbase + C::kOffK + ks * C::kTileBytes + s * C::kSlabBytes, &tm_k,
+                            bar(C::kBarKF + ks), s * 64, j * 128, zkv);
         for (int s = 0; s < C::kSlabs; ++s)
           tma_load_3d_elect(sbase + C::kOffV + vs * C::kTileBytes + s * C::kSlabBytes, &tm_v,
-                            bar(C::kBarVF + vs), s * 64, j * 128, zkv);
-        v_issued = j + 1;
+                            bar(C::kBarKF + ks), s * 64, j * 128, zkv);
+        issued = j + 1;
       }
       if (!ok) {
         const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
-        for (int j = max(0, k_issued - C::kKStages); j < k_issued; ++j)
+        for (int j = max(0, issued - C::kKStages); j < issued; ++j)
           mbar_wait_drain(bar(C::kBarKF + j % C::kKStages), (j / C::kKStages) & 1, deadline);
-        for (int j = max(0, v_issued - C::kVStages); j < v_issued; ++j)
-          mbar_wait_drain(bar(C::kBarVF + j % C::kVStages), (j / C::kVStages) & 1, deadline);
       }
     } else if (warp == 1 && n > 0) {
       // ------------------------------------------------------ MMA issuer
@@ -299,9 +298,6 @@ __global__ void __launch_bounds__(384, 1)
       for (int j = 0; ok && j < n; ++j) {
         const int ks = j % C::kKStages, vs = j % C::kVStages;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarKF + ks), (j / C::kKStages) & 1,
-                                               abort_flag, err, kErrTimeoutMma));
-        if (!ok) break;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarVF + vs), (j / C::kVStages) & 1,
                                                abort_flag, err, kErrTimeoutMma));
         if (!ok) break;
         tc_fence_after();
