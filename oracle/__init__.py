@@ -39,7 +39,7 @@ from .attention import (
     attention_ref,
     attention_online,
 )
-from .backward import attention_bwd_ref
+from .backward import attention_bwd_ref, attention_bwd_rows
 from .kv_cache import BlockManagerRef, append_logical
 from .paged import gather_logical_kv, paged_decode_ref, paged_decode_ref_from_pool, paged_prefill_ref
 
@@ -55,6 +55,7 @@ __all__ = [
     "paged_decode_ref_from_pool",
     "paged_prefill_ref",
     "attention_bwd_ref",
+    "attention_bwd_rows",
     "append_logical",
     "BlockManagerRef",
 ]

@@ -71,3 +71,65 @@ def attention_bwd_ref(q: np.ndarray, k: np.ndarray, v: np.ndarray, do: np.ndarra
             dk[b, g] += scale * (dS.T @ q[b, h])
             D[b, h] = Dh
     return dq, dk, dv, D
+
+
+def attention_bwd_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, do: np.ndarray,
+                       scale: float, causal: bool, q_rows, key_rows, kv_heads,
+                       row_slice: int = 1024):
+    """The same gradients as ``attention_bwd_ref``, evaluated only where asked.
+
+    For sizes where the full N x N matrices do not fit (a 16k-token context),
+    this returns
+      dq  [B, H, len(q_rows), d]        the rows ``q_rows`` of dQ, every head;
+      dk, dv [len(kv_heads), len(key_rows), d]
+                                        the rows ``key_rows`` of dK and dV for
+                                        each (b, kv head) pair in ``kv_heads``.
+    The arithmetic is the chain rule written out in ``attention_bwd_ref``:
+
+    * a dQ row i needs the full row i of P (the softmax over all its keys),
+      the full row of dP = dO_i V^T, D_i = sum_j P_ij dP_ij, and then
+      dQ_i = scale sum_j P_ij (dP_ij - D_i) K_j;
+    * a dK / dV row j needs column j of P and dP for every query of every
+      head that reads the KV head, and each query's D_i, which needs that
+      query's whole row: dV_j = sum_i P_ij dO_i, dK_j = scale sum_i
+      P_ij (dP_ij - D_i) Q_i, summed over the heads of the group.
+
+    Query rows are evaluated ``row_slice`` at a time only to bound memory;
+    every row's softmax and D are taken over the full row, as in the
+    definition.  q, k, v, do float64 as for ``attention_bwd_ref``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    B, H, Hkv, Nq, Nk, d = _check_shapes(q, k, v)
+    if do.shape != q.shape:
+        raise ValueError("do must have q's shape")
+    G = H // Hkv
+    qr = np.asarray(q_rows, dtype=np.int64)
+    kr = np.asarray(key_rows, dtype=np.int64)
+    dq = np.zeros((B, H, qr.shape[0], d))
+    for b in range(B):
+        for h in range(H):
+            g = h // G
+            S = scores(q[b, h, qr], k[b, g], scale, causal, qr, Nq)
+            P, _, _ = softmax_rows(S)
+            dP = do[b, h, qr] @ v[b, g].T
+            Dh = np.sum(P * dP, axis=1)
+            dq[b, h] = scale * ((P * (dP - Dh[:, None])) @ k[b, g])
+    pairs = [(int(b), int(g)) for b, g in kv_heads]
+    dk = np.zeros((len(pairs), kr.shape[0], d))
+    dv = np.zeros((len(pairs), kr.shape[0], d))
+    for n, (b, g) in enumerate(pairs):
+        for h in range(g * G, (g + 1) * G):
+            for i0 in range(0, Nq, row_slice):
+                rows = np.arange(i0, min(Nq, i0 + row_slice))
+                S = scores(q[b, h, rows], k[b, g], scale, causal, rows, Nq)
+                P, _, _ = softmax_rows(S)
+                dP = do[b, h, rows] @ v[b, g].T
+                Dh = np.sum(P * dP, axis=1)
+                Pc = P[:, kr]
+                dSc = Pc * (dP[:, kr] - Dh[:, None])
+                dv[n] += Pc.T @ do[b, h, rows]
+                dk[n] += scale * (dSc.T @ q[b, h, rows])
+    return dq, dk, dv

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from attention_fa_attn_fwd_b300 import binding, workloads
-from tests.parity import compare_grad, f64
+from tests.parity import compare_grad, f64, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -88,3 +88,27 @@ def test_deterministic_and_status_clean():
     torch.cuda.synchronize()
     assert all(torch.equal(x, y) for x, y in zip(a, b))
     assert binding.device_status() == binding.ATTN_OK
+
+
+def test_long_context_gqa_sampled():
+    """The long-context causal GQA workload the backward is timed on
+    (B1 H32 Hkv8 N16384 d128, Q and K x1.5): dQ on 64 seeded query rows of
+    every head, dK and dV on 64 seeded key rows of two seeded KV groups.
+    Every key row's gradient sums over all 16384 queries of the 4 heads of its
+    group, so this covers the long accumulation in dK/dV, the multi-wave grids
+    and the long key loop of dQ."""
+    cfg = workloads.PREFILL_WORKLOADS["gqa_b1h32kv8_n16384_d128_causal"]
+    q, k, v = workloads.prefill_inputs(**cfg)
+    do = workloads.grad_output(q.shape, seed=0)
+    N, d = cfg["Nq"], cfg["d"]
+    dq, dk, dv = _run(q, k, v, do, True)
+    qr = sample_rows(N, 64, seed=101)
+    kr = sample_rows(N, 64, seed=102)
+    groups = sorted(np.random.default_rng(103).choice(cfg["Hkv"], size=2, replace=False).tolist())
+    pairs = [(0, g) for g in groups]
+    rq, rk, rv = oracle.attention_bwd_rows(f64(q), f64(k), f64(v), f64(do), 1 / math.sqrt(d),
+                                           True, qr, kr, pairs)
+    compare_grad(f64(dq[:, :, qr]), rq, "dq long-context (64 rows x 32 heads)")
+    for n, (b, g) in enumerate(pairs):
+        compare_grad(f64(dk[b, g, kr]), rk[n], f"dk long-context group {g} (64 rows)")
+        compare_grad(f64(dv[b, g, kr]), rv[n], f"dv long-context group {g} (64 rows)")

@@ -148,3 +148,48 @@ def test_pins_catch_backward_mutant(kind):
 def test_mutant_harness_passes_when_correct():
     for pin in BACKWARD_PINS:
         pin(_mutant("none"))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,Hkv,Nq,Nk,d,row_slice", [(1, 4, 2, 9, 9, 4, 4), (2, 6, 3, 7, 11, 3, 3),
+                                                      (1, 2, 1, 12, 5, 5, 5), (1, 4, 1, 6, 6, 8, 100)])
+def test_rows_variant_equals_autograd_rows(causal, B, H, Hkv, Nq, Nk, d, row_slice):
+    """attention_bwd_rows on chosen rows equals float64 torch autograd through
+    scaled_dot_product_attention (a library special case, independent of the
+    oracle) on the same rows, and the full chain-rule oracle."""
+    rng = np.random.default_rng(Nq * 31 + Nk + d)
+    q = rng.standard_normal((B, H, Nq, d))
+    k = rng.standard_normal((B, Hkv, Nk, d))
+    v = rng.standard_normal((B, Hkv, Nk, d))
+    do = rng.standard_normal((B, H, Nq, d))
+    scale = 0.6
+    qr = np.array(sorted(rng.choice(Nq, size=min(Nq, 4), replace=False)))
+    kr = np.array(sorted(rng.choice(Nk, size=min(Nk, 3), replace=False)))
+    pairs = [(b, g) for b in range(B) for g in range(Hkv)][::-1]
+    dq, dk, dv = oracle.attention_bwd_rows(q, k, v, do, scale, causal, qr, kr, pairs,
+                                           row_slice=row_slice)
+    # torch's is_causal is top-left aligned; build the bottom-right mask explicitly
+    G = H // Hkv
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    mask = None
+    if causal:
+        i = torch.arange(Nq)[:, None]
+        j = torch.arange(Nk)[None, :]
+        allowed = j <= i + (Nk - Nq)
+        mask = torch.where(allowed, 0.0, float("-inf")).double()
+    o = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk.repeat_interleave(G, dim=1), tv.repeat_interleave(G, dim=1), attn_mask=mask,
+        scale=scale)
+    # rows with no key give NaN in torch; their gradient is 0 by the reading
+    o = torch.nan_to_num(o)
+    o.backward(torch.tensor(do))
+    gq, gk, gv = (torch.nan_to_num(t.grad).numpy() for t in (tq, tk, tv))
+    assert np.max(np.abs(dq - gq[:, :, qr])) <= 1e-10
+    for n, (b, g) in enumerate(pairs):
+        assert np.max(np.abs(dk[n] - gk[b, g, kr])) <= 1e-10
+        assert np.max(np.abs(dv[n] - gv[b, g, kr])) <= 1e-10
+    fq, fk, fv, _ = oracle.attention_bwd_ref(q, k, v, do, scale, causal)
+    assert np.max(np.abs(dq - fq[:, :, qr])) <= 1e-12
+    for n, (b, g) in enumerate(pairs):
+        assert np.max(np.abs(dk[n] - fk[b, g, kr])) <= 1e-12
+        assert np.max(np.abs(dv[n] - fv[b, g, kr])) <= 1e-12
