@@ -26,6 +26,7 @@ ATTN_EUNSUPPORTED = 2
 ATTN_ECUDA = 3
 ATTN_EDEVICE = 4
 ATTN_FWD_EXP2_FMA = 1  # attn_fwd_ex flag
+ATTN_BWD_DETERMINISTIC = 1  # attn_bwd_ex flag
 _STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_EINVAL", 2: "ATTN_EUNSUPPORTED",
                  3: "ATTN_ECUDA", 4: "ATTN_EDEVICE"}
 
@@ -48,9 +49,11 @@ SIGNATURES = {
                                   _vp, _vp, _vp]),
     "paged_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
                            _vp, _vp, _vp]),
-    "attn_bwd_workspace_size": (_sz, [_i, _i, _i]),
+    "attn_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
     "attn_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i,
                       _vp, _sz, _vp]),
+    "attn_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,
+                         _i, _vp, _sz, ctypes.c_uint, _vp]),
     "kv_append_workspace_size": (_sz, [_i, _i]),
     "kv_append": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                        _vp, _sz, _vp]),
@@ -234,12 +237,14 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              do: torch.Tensor, lse: torch.Tensor, causal: bool = False,
              scale: Optional[float] = None, dq: Optional[torch.Tensor] = None,
              dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
-             workspace: Optional[torch.Tensor] = None, stream=None):
-    """Gradients (dq, dk, dv) of ``attn_fwd`` via ``attn_bwd``.
+             workspace: Optional[torch.Tensor] = None, stream=None,
+             deterministic: bool = False):
+    """Gradients (dq, dk, dv) of ``attn_fwd`` via ``attn_bwd_ex``.
 
     q, o, do [B,H,Nq,d] bf16; k, v [B,Hkv,Nk,d] bf16; lse [B,H,Nq] fp32 from
     ``attn_fwd``.  ``workspace``: uint8 CUDA tensor of at least
     ``attn_bwd_workspace_size`` bytes (allocated here if omitted).
+    ``deterministic`` sets ATTN_BWD_DETERMINISTIC (bit-reproducible dq).
     """
     lib = load_library()
     for t, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
@@ -259,21 +264,22 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
         _need(t, name, torch.bfloat16, 4)
         if t.shape != ref.shape:
             raise ValueError(f"{name} has the wrong shape")
-    need = int(lib.attn_bwd_workspace_size(B, H, Nq))
+    need = int(lib.attn_bwd_workspace_size(B, H, Nq, d))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     elif workspace.dtype != torch.uint8 or not workspace.is_cuda:
         raise TypeError("workspace must be a uint8 CUDA tensor")
-    st = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                      lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                      B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
-                      workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    flags = ATTN_BWD_DETERMINISTIC if deterministic else 0
+    st = lib.attn_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                         lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                         B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                         workspace.data_ptr(), workspace.numel(), flags, _stream_handle(stream))
     _check(st)
     return dq, dk, dv
 
 
-def attn_bwd_workspace_size(B: int, H: int, Nq: int) -> int:
-    return int(load_library().attn_bwd_workspace_size(B, H, Nq))
+def attn_bwd_workspace_size(B: int, H: int, Nq: int, d: int) -> int:
+    return int(load_library().attn_bwd_workspace_size(B, H, Nq, d))
 
 
 def paged_decode_workspace_size(num_seqs: int, H: int, Hkv: int, d: int,

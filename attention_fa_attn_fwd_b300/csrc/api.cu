@@ -231,15 +231,16 @@ attn_status paged_prefill(const void* q, const void* k_cache, const void* v_cach
   return ATTN_OK;
 }
 
-size_t attn_bwd_workspace_size(int B, int H, int Nq) {
-  if (B < 1 || H < 1 || Nq < 1) return 0;
-  return attn::backward_workspace_bytes(B, H, Nq);
+size_t attn_bwd_workspace_size(int B, int H, int Nq, int d) {
+  if (B < 1 || H < 1 || Nq < 1 || (d != 64 && d != 128)) return 0;
+  return attn::backward_workspace_bytes(B, H, Nq, d, false);
 }
 
-attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq,
-                     int Nk, int d, float scale, int causal, void* workspace,
-                     size_t workspace_bytes, attn_stream_t stream) {
+attn_status attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                        int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                        void* workspace, size_t workspace_bytes, unsigned flags,
+                        attn_stream_t stream) {
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
     return fail(ATTN_EINVAL, "attn_bwd: null pointer argument");
   if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < 1)
@@ -249,6 +250,8 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   if (!(scale > 0.f) || !(scale < 3.0e38f))
     return fail(ATTN_EINVAL, "attn_bwd: scale must be positive and finite");
   if (causal != 0 && causal != 1) return fail(ATTN_EINVAL, "attn_bwd: causal must be 0 or 1");
+  if (flags & ~unsigned(ATTN_BWD_DETERMINISTIC))
+    return fail(ATTN_EINVAL, "attn_bwd: unknown flags 0x%x", flags);
   if (d != 64 && d != 128) return fail(ATTN_EUNSUPPORTED, "attn_bwd: head dim %d (need 64 or 128)", d);
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
@@ -257,18 +260,27 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   if ((long long)B * H * ((Nq + 127) / 128) >= (1LL << 31) ||
       (long long)B * Hkv * ((Nk + 127) / 128) >= (1LL << 31))
     return fail(ATTN_EINVAL, "attn_bwd: problem too large");
-  const size_t need = attn::backward_workspace_bytes(B, H, Nq);
+  const bool det = (flags & ATTN_BWD_DETERMINISTIC) != 0;
+  const size_t need = attn::backward_workspace_bytes(B, H, Nq, d, det);
   if (workspace_bytes < need)
     return fail(ATTN_EINVAL, "attn_bwd: workspace %zu bytes < required %zu", workspace_bytes, need);
   attn_status st = check_device();
   if (st != ATTN_OK) return st;
   const char* err = nullptr;
   cudaError_t e = attn::backward_launch(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, Nq, Nk, d,
-                                        scale, causal, workspace,
+                                        scale, causal, det, workspace,
                                         reinterpret_cast<cudaStream_t>(stream), &err);
   if (err) return fail(ATTN_ECUDA, "attn_bwd: %s", err);
   if (e != cudaSuccess) return fail(ATTN_ECUDA, "attn_bwd launch: %s", cudaGetErrorString(e));
   return ATTN_OK;
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq,
+                     int Nk, int d, float scale, int causal, void* workspace,
+                     size_t workspace_bytes, attn_stream_t stream) {
+  return attn_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, Nq, Nk, d, scale, causal,
+                     workspace, workspace_bytes, 0u, stream);
 }
 
 size_t kv_append_workspace_size(int num_seqs, int num_blocks) {

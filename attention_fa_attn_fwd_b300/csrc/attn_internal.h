@@ -47,11 +47,12 @@ cudaError_t decode_launch(const void* q, const void* k_cache, const void* v_cach
 int decode_take_device_error();
 
 // ---- backward (backward_sm103.cu)
-size_t backward_workspace_bytes(int B, int H, int Nq);
+size_t backward_workspace_bytes(int B, int H, int Nq, int d, bool deterministic);
 cudaError_t backward_launch(const void* q, const void* k, const void* v, const void* o,
                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
                             int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
-                            void* workspace, cudaStream_t stream, const char** err);
+                            bool deterministic, void* workspace, cudaStream_t stream,
+                            const char** err);
 int backward_take_device_error();
 
 // ---- paged-cache append (kv_append.cu)

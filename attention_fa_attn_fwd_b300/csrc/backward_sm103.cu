@@ -113,15 +113,17 @@ __device__ __forceinline__ float neg_lse2_of(float lse) {
 
 // ================================================================ delta
 // D[row] = sum_c dO[row, c] * O[row, c]; D/8 threads per row, 16-byte loads.
+// If acc is given, the row's D fp32 dQ accumulator entries are zeroed too.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restrict__ o,
                                                         const uint16_t* __restrict__ dout,
-                                                        float* __restrict__ delta, long long rows) {
+                                                        float* __restrict__ delta, long long rows,
+                                                        float* __restrict__ acc) {
   constexpr int TPR = D / 8;  // threads per row
   const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = t / TPR;
   const int part = int(t % TPR);
-  float acc = 0.f;
+  float sum = 0.f;
   if (row < rows) {
     const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + part * 8);
     const uint4 b = *reinterpret_cast<const uint4*>(dout + row * D + part * 8);
@@ -129,13 +131,18 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restri
     const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      acc += __uint_as_float(av[e] << 16) * __uint_as_float(bv[e] << 16);
-      acc += __uint_as_float(av[e] & 0xffff0000u) * __uint_as_float(bv[e] & 0xffff0000u);
+      sum += __uint_as_float(av[e] << 16) * __uint_as_float(bv[e] << 16);
+      sum += __uint_as_float(av[e] & 0xffff0000u) * __uint_as_float(bv[e] & 0xffff0000u);
+    }
+    if (acc) {
+      float4* z = reinterpret_cast<float4*>(acc + row * D + part * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 #pragma unroll
-  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && part == 0) delta[row] = acc;
+  for (int off = TPR / 2; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (row < rows && part == 0) delta[row] = sum;
 }
 
 // ================================================================ dQ
@@ -767,6 +774,421 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// ================================================================ fused (d = 128)
+// One KV-stationary kernel for all five products.  A CTA owns 128 keys of
+// one KV head and streams the 64-query halves of every (query head, query
+// tile) that sees them, as bwd_dkdv_kernel does, and also forms this key
+// tile's share of dQ:
+//   dQ^T_u = K^T dS^T_u   (M = d = 128, N = 64 queries, K = 128 keys)
+// from the bf16 dS^T the compute warpgroup writes to shared memory.  dQ^T
+// lands in the half's dP^T columns of TMEM (free once the compute
+// warpgroup has read them); a fourth warpgroup reads it out (lane = d, so a
+// warp's 32 lanes cover 32 consecutive floats of one query row) and adds it
+// to an fp32 dQ accumulator in the workspace with coalesced atomic adds in
+// L2.  A conversion kernel then writes dq = bf16(scale * accumulator).  The
+// adds from different key tiles arrive in no fixed order, so dq can differ
+// between calls by fp32 rounding; dk and dv are accumulated in TMEM in a
+// fixed order and are bit-reproducible.
+//
+// Warps: 0 TMA producer, 1 MMA issuer, 2-3 idle, 4-7 compute half 0,
+// 8-11 compute half 1, 12-15 dQ drain.
+struct FusedCfg : BCfg<128> {
+  using B_ = BCfg<128>;
+  static constexpr int kHalfSlabBytes = 64 * 128;
+  static constexpr int kHalfBytes = B_::kSlabs * kHalfSlabBytes;  // 64 rows x 128 bf16
+  static constexpr int kHS = 3;                                   // Q / dO half-stages
+  static constexpr int kDSBytes = 128 * 128;                      // dS^T: 128 keys x 64 q bf16
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = B_::kTileBytes;
+  static constexpr int kOffQ = 2 * B_::kTileBytes;
+  static constexpr int kOffDO = kOffQ + kHS * kHalfBytes;
+  static constexpr int kOffDS = kOffDO + kHS * kHalfBytes;        // 2 dS^T tiles (one per half)
+  static constexpr int kOffStat = kOffDS + 2 * kDSBytes;          // [hs][2][64] fp32
+  static constexpr int kOffBar = kOffStat + kHS * 2 * 64 * 4;
+  static constexpr int kBarKVF = 0;
+  static constexpr int kBarQF = 1;                 // kHS (32 arrivals + tx)
+  static constexpr int kBarQE = kBarQF + kHS;      // kHS
+  static constexpr int kBarSF = kBarQE + kHS;      // 2: S^T_h, dP^T_h in TMEM
+  static constexpr int kBarPF = kBarSF + 2;        // 2: P^T_h, dS^T_h written (128 arrivals)
+  static constexpr int kBarDQF = kBarPF + 2;       // 2: dQ^T_h in TMEM
+  static constexpr int kBarDQE = kBarDQF + 2;      // 2: dQ^T_h read out (128 arrivals)
+  static constexpr int kBarOF = kBarDQE + 2;       // dK, dV complete
+  static constexpr int kBarDrain = kBarOF + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  // half h: S^T_h at h*128 (64 columns; P^T_h then dS^T_h as bf16 pairs over
+  // its first 32 and second 32), dP^T_h at h*128 + 64 (then dQ^T_h).
+  static constexpr uint32_t kColDV = 256, kColDK = 384;
+  static constexpr int kRegsLow = 72, kRegsDrain = 72, kRegsHigh = 176;
+  static_assert(kHS * kHalfBytes >= B_::kTileBytes, "epilogue staging needs one tile");
+  static_assert(kRegsLow * 128 + kRegsDrain * 128 + kRegsHigh * 256 <= 65536, "register split");
+};
+
+__global__ void __launch_bounds__(512, 1)
+    bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_dk,
+                     const __grid_constant__ CUtensorMap tm_dv, const BArgs a, float* dq_acc) {
+  using C = FusedCfg;
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  float* stat = reinterpret_cast<float*>(smem + C::kOffStat);
+  int* err = &g_backward_error;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // CTA = (b, KV head, key tile); key tiles of one head adjacent (L2 reuse of
+  // the group's Q / dO and of its dQ accumulator rows).
+  const int n_kt = (a.Nk + 127) / 128;
+  const int zkv = blockIdx.x / n_kt;
+  const int k0 = int(blockIdx.x % n_kt) * 128;
+  const int b = zkv / a.Hkv, g = zkv % a.Hkv;
+  const int G = a.H / a.Hkv;
+  const int off = a.Nk - a.Nq;
+  const int n_qt = (a.Nq + 127) / 128;
+  int qt0 = 0;
+  if (a.causal) {
+    const int first_row = k0 - off;
+    qt0 = first_row <= 0 ? 0 : first_row / 128;
+  }
+  const bool dead = timed_out_before(err);
+  const int per_head = max(0, n_qt - qt0);
+  const int n_it = dead ? 0 : G * per_head;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i) {
+      uint32_t cnt = 1;
+      if (i == C::kBarPF || i == C::kBarPF + 1 || i == C::kBarDQE || i == C::kBarDQE + 1) cnt = 128;
+      if (i >= C::kBarQF && i < C::kBarQF + C::kHS) cnt = 32;
+      mbar_init(bar(i), cnt);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_do);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_dk);
+    prefetch_tmap(&tm_dv);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    setmaxnreg_dec<C::kRegsLow>();
+    if (warp == 0 && n_it > 0) {
+      // ------------------------------------------------------ producer
+      mbar_arrive_expect_tx_elect(bar(C::kBarKVF), 2 * C::kTileBytes);
+      for (int s = 0; s < C::kSlabs; ++s) {
+        tma_load_3d_elect(sbase + C::kOffK + s * C::kSlabBytes, &tm_k, bar(C::kBarKVF), s * 64, k0,
+                          zkv);
+        tma_load_3d_elect(sbase + C::kOffV + s * C::kSlabBytes, &tm_v, bar(C::kBarKVF), s * 64, k0,
+                          zkv);
+      }
+      bool ok = true;
+      int issued = 0;
+      for (int u = 0; u < 2 * n_it; ++u) {
+        const int it = u >> 1, h = u & 1;
+        const int hs = u % C::kHS;
+        const int hq = b * a.H + g * G + it / per_head;
+        const int r0 = (qt0 + it % per_head) * 128 + h * 64;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarQE + hs), ((u / C::kHS) & 1) ^ 1,
+                                               abort_flag, err, kErrTimeoutProducer));
+        if (!ok) break;
+        float* sp = stat + hs * 128;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int cidx = lane * 2 + e;
+          const int r = r0 + cidx;
+          float nl = -INFINITY, dd = 0.f;
+          if (r < a.Nq) {
+            nl = neg_lse2_of(a.lse[size_t(hq) * a.Nq + r]);
+            dd = a.delta[size_t(hq) * a.Nq + r];
+          }
+          sp[cidx] = nl;
+          sp[64 + cidx] = dd;
+        }
+        if (lane == 0)
+          mbar_arrive_expect_tx(bar(C::kBarQF + hs), 2 * C::kHalfBytes);
+        else
+          mbar_arrive(bar(C::kBarQF + hs));
+        __syncwarp();
+        for (int s = 0; s < C::kSlabs; ++s) {
+          tma_load_3d_elect(sbase + C::kOffQ + hs * C::kHalfBytes + s * C::kHalfSlabBytes, &tm_q,
+                            bar(C::kBarQF + hs), s * 64, r0, hq);
+          tma_load_3d_elect(sbase + C::kOffDO + hs * C::kHalfBytes + s * C::kHalfSlabBytes, &tm_do,
+                            bar(C::kBarQF + hs), s * 64, r0, hq);
+        }
+        issued = u + 1;
+      }
+      if (!ok) {
+        const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
+        mbar_wait_drain(bar(C::kBarKVF), 0, deadline);
+        for (int u = max(0, issued - C::kHS); u < issued; ++u)
+          mbar_wait_drain(bar(C::kBarQF + u % C::kHS), (u / C::kHS) & 1, deadline);
+      }
+    } else if (warp == 1 && n_it > 0) {
+      // ------------------------------------------------------ MMA issuer
+      constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, 0);
+      constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 1);
+      constexpr uint32_t kIdescDQ = idesc_bf16_f32_amn(128, 64, 1);
+      const uint64_t k_desc = smem_desc_sw128(sbase + C::kOffK, 16, 1024);
+      const uint64_t v_desc = smem_desc_sw128(sbase + C::kOffV, 16, 1024);
+      const uint64_t q_desc = smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
+      const uint64_t do_desc = smem_desc_sw128(sbase + C::kOffDO, 16, 1024);
+      const uint64_t qmn_desc = smem_desc_sw128(sbase + C::kOffQ, C::kHalfSlabBytes, 1024);
+      const uint64_t domn_desc = smem_desc_sw128(sbase + C::kOffDO, C::kHalfSlabBytes, 1024);
+      // K^T as an MN-major A operand (M = d: 64-column slabs kSlabBytes
+      // apart); dS^T as an MN-major B operand (N = 64 queries, one atom).
+      const uint64_t kmn_desc = smem_desc_sw128(sbase + C::kOffK, C::kSlabBytes, 1024);
+      const uint64_t ds_desc = smem_desc_sw128(sbase + C::kOffDS, C::kDSBytes, 1024);
+      // S^T_h = K Q[u]^T over the 64 queries of half u: two chains of four
+      // K-steps (32 bytes apart inside a 64-column slab; the second chain in
+      // the next slab).  Operand offsets are added inside the asm so the
+      // descriptors stay in a few registers.
+      auto issue_s = [&](int u) -> bool {
+        const int h = u & 1, hs = u % C::kHS;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarQF + hs), (u / C::kHS) & 1, abort_flag,
+                                               err, kErrTimeoutMma)))
+          return false;
+        tc_fence_after();
+        const uint64_t qd = q_desc + uint64_t((hs * C::kHalfBytes) >> 4);
+        mma4_bf16_ss<2, 2>(tmem + h * 128, k_desc, qd, kIdescHalf, 0u);
+        mma4_bf16_ss<2, 2>(tmem + h * 128, k_desc + (C::kSlabBytes >> 4),
+                           qd + (C::kHalfSlabBytes >> 4), kIdescHalf, 1u);
+        return true;
+      };
+      // dP^T_h = V dO[u]^T into the half's second 64 columns, which hold
+      // dQ^T of half u - 2 until the drain warpgroup has read it.
+      auto issue_dp = [&](int u) -> bool {
+        const int h = u & 1, hs = u % C::kHS;
+        if (u >= 2) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarDQE + h), ((u >> 1) - 1) & 1,
+                                                 abort_flag, err, kErrTimeoutMma)))
+            return false;
+          tc_fence_after();
+        }
+        const uint64_t dd = do_desc + uint64_t((hs * C::kHalfBytes) >> 4);
+        mma4_bf16_ss<2, 2>(tmem + h * 128 + 64, v_desc, dd, kIdescHalf, 0u);
+        mma4_bf16_ss<2, 2>(tmem + h * 128 + 64, v_desc + (C::kSlabBytes >> 4),
+                           dd + (C::kHalfSlabBytes >> 4), kIdescHalf, 1u);
+        mma_commit(bar(C::kBarSF + h));
+        return true;
+      };
+      // dV += P^T_h dO[u], dK += dS^T_h Q[u] (frees the half-stage), then
+      // dQ^T_h = K^T dS^T_h (16 keys = 2048 bytes per MMA in both operands).
+      auto issue_acc = [&](int u) -> bool {
+        const int h = u & 1, hs = u % C::kHS;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF + h), (u >> 1) & 1, abort_flag, err,
+                                               kErrTimeoutMma)))
+          return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t o16 = uint32_t((hs * C::kHalfBytes + kk * 16 * 128) >> 4);
+          const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
+          mma_bf16_ts(tmem + C::kColDV, tmem + h * 128 + kk * 8, desc_add(domn_desc, o16), kIdescAcc,
+                      acc);
+          mma_bf16_ts(tmem + C::kColDK, tmem + h * 128 + 32 + kk * 8, desc_add(qmn_desc, o16),
+                      kIdescAcc, acc);
+        }
+        mma_commit(bar(C::kBarQE + hs));
+        const uint64_t dsd = ds_desc + uint64_t((h * C::kDSBytes) >> 4);
+        mma4_bf16_ss<128, 128>(tmem + h * 128 + 64, kmn_desc, dsd, kIdescDQ, 0u);
+        mma4_bf16_ss<128, 128>(tmem + h * 128 + 64, kmn_desc + 512, dsd + 512, kIdescDQ, 1u);
+        mma_commit(bar(C::kBarDQF + h));
+        return true;
+      };
+      bool ok = __all_sync(0xffffffffu,
+                           mbar_wait(bar(C::kBarKVF), 0, abort_flag, err, kErrTimeoutMma));
+      // Per (query head, query tile) it: S(u0) dP(u0) [acc(u0 - 1)] S(u1) dP(u1) acc(u0).
+      for (int it = 0; ok && it < n_it; ++it) {
+        ok = issue_s(2 * it);
+        if (ok) ok = issue_dp(2 * it);
+        if (ok && it > 0) ok = issue_acc(2 * it - 1);
+        if (ok) ok = issue_s(2 * it + 1);
+        if (ok) ok = issue_dp(2 * it + 1);
+        if (ok) ok = issue_acc(2 * it);
+      }
+      if (ok && n_it > 0) ok = issue_acc(2 * n_it - 1);
+      if (ok) {
+        mma_commit(bar(C::kBarOF));
+      } else {
+        mma_commit(bar(C::kBarDrain));
+        mbar_wait_drain(bar(C::kBarDrain), 0, globaltimer_ns() + kWaitTimeoutNs);
+      }
+    }
+  } else if (warp >= 12) {
+    setmaxnreg_dec<C::kRegsDrain>();
+    // -------------------------------------------------------- dQ drain
+    const int quarter = warp & 3;
+    const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
+    const int dcol = quarter * 32 + lane;
+    bool ok = !dead;
+    for (int u = 0; ok && u < 2 * n_it; ++u) {
+      const int it = u >> 1, h = u & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarDQF + h), (u >> 1) & 1, abort_flag, err,
+                                             kErrTimeoutEpilogue));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld32(lane_base + h * 128 + 64, v);
+      tmem_ld32(lane_base + h * 128 + 96, v + 32);
+      tmem_ld_wait();
+      reg_fence<64>(v);
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarDQE + h));
+      const int hq = b * a.H + g * G + it / per_head;
+      const int r0 = (qt0 + it % per_head) * 128 + h * 64;
+      const int nrow = min(64, a.Nq - r0);
+      float* dst = dq_acc + (size_t(hq) * a.Nq + r0) * D + dcol;
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        if (j < nrow) atomicAdd(dst + size_t(j) * D, __uint_as_float(v[j]));
+    }
+  } else {
+    setmaxnreg_inc<C::kRegsHigh>();
+    // -------------------------------------------------------- compute
+    const int wg = (warp >> 2) - 1;  // which 64-query half of the tile
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // key within the tile
+    const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
+    const int kj = k0 + row;
+    const float c = a.c_log2;
+    uint8_t* ds_row = smem + C::kOffDS + wg * C::kDSBytes + row * 128;
+    bool ok = !dead;
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int u = 2 * it + wg, hs = u % C::kHS;
+      const int r0 = (qt0 + it % per_head) * 128;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarQF + hs), (u / C::kHS) & 1,
+                                             abort_flag, err, kErrTimeoutSoftmax));
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::kBarSF + wg), it & 1, abort_flag, err, kErrTimeoutSoftmax));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[64], p[64];
+      tmem_ld32(lane_base + wg * 128, s);
+      tmem_ld32(lane_base + wg * 128 + 32, s + 32);
+      tmem_ld32(lane_base + wg * 128 + 64, p);
+      tmem_ld32(lane_base + wg * 128 + 96, p + 32);
+      tmem_ld_wait();
+      reg_fence<64>(s);
+      reg_fence<64>(p);
+      const float* nl = stat + hs * 128;
+      const float* dd = nl + 64;
+      const int lo = a.causal ? (kj - off - r0 - wg * 64) : -1;
+      const bool key_ok = kj < a.Nk;
+      const bool masked = !key_ok || lo > 0;
+      const float2 c2 = make_float2(c, c);
+      const float2* nl2 = reinterpret_cast<const float2*>(nl);
+      const float2* dd2 = reinterpret_cast<const float2*>(dd);
+      uint32_t pp[32], pd[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])),
+                              c2, nl2[e]);
+        x.x = ex2_approx(x.x);
+        x.y = ex2_approx(x.y);
+        if (masked) {
+          if (!key_ok || 2 * e < lo) x.x = 0.f;
+          if (!key_ok || 2 * e + 1 < lo) x.y = 0.f;
+        }
+        pp[e] = pack_bf16x2(x.x, x.y);
+        const float2 ndd = dd2[e];
+        const float2 dp = __fadd2_rn(make_float2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])),
+                                     make_float2(-ndd.x, -ndd.y));
+        const float2 d = __fmul2_rn(x, dp);
+        pd[e] = pack_bf16x2(d.x, d.y);
+      }
+      // dS^T row (this key, 64 queries = 128 bytes) into the half's shared
+      // tile, 128-byte swizzled: the B operand of dQ^T.
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(ds_row + ((ch ^ (row & 7)) << 4)) =
+            make_uint4(pd[4 * ch], pd[4 * ch + 1], pd[4 * ch + 2], pd[4 * ch + 3]);
+      tmem_st32(lane_base + wg * 128, pp);
+      tmem_st32(lane_base + wg * 128 + 32, pd);
+      fence_proxy_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarPF + wg));
+    }
+    // -------------------------------------------------------- epilogue
+    if (ok && n_it > 0) {
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::kBarOF), 0, abort_flag, err, kErrTimeoutEpilogue));
+      tc_fence_after();
+    }
+    uint8_t* stage = smem + (wg == 0 ? C::kOffQ : C::kOffDO);
+    const uint32_t col = wg == 0 ? C::kColDV : C::kColDK;
+    const float mul = wg == 0 ? 1.f : a.scale;
+    if (ok) {
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t v[32];
+        if (n_it > 0) {
+          tmem_ld32(lane_base + col + c0, v);
+          tmem_ld_wait();
+          reg_fence<32>(v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        stage_row32<D>(stage, row, c0, v, mul);
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1 + wg, 128);
+    if (!*abort_flag && ok && quarter == 0 && lane == 0) {
+      const CUtensorMap* tm = wg == 0 ? &tm_dv : &tm_dk;
+      const uint32_t src = sbase + (wg == 0 ? C::kOffQ : C::kOffDO);
+      for (int s = 0; s < C::kSlabs; ++s)
+        tma_store_3d(tm, src + s * C::kSlabBytes, s * 64, k0, zkv);
+      bulk_commit_group();
+      bulk_wait_group_read0();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// dq = bf16(scale * accumulator), 8 elements per thread.
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ acc,
+                                                             uint16_t* __restrict__ dq,
+                                                             long long n8, float scale) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n8) return;
+  const float4 x = reinterpret_cast<const float4*>(acc)[2 * t];
+  const float4 y = reinterpret_cast<const float4*>(acc)[2 * t + 1];
+  uint4 r;
+  r.x = pack_bf16x2(x.x * scale, x.y * scale);
+  r.y = pack_bf16x2(x.z * scale, x.w * scale);
+  r.z = pack_bf16x2(y.x * scale, y.y * scale);
+  r.w = pack_bf16x2(y.z * scale, y.w * scale);
+  reinterpret_cast<uint4*>(dq)[t] = r;
+}
+
 // ================================================================ launch
 
 template <typename K>
@@ -786,27 +1208,23 @@ template <int D>
 cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o,
                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
                        int H, int Hkv, int Nq, int Nk, float scale, int causal, float* delta,
-                       cudaStream_t stream, const char** err) {
+                       float* dq_acc, cudaStream_t stream, const char** err) {
   const uint32_t box[3] = {64, 128, 1};
   const uint64_t dq_[3] = {uint64_t(D), uint64_t(Nq), uint64_t(B) * H};
   const uint64_t sq[2] = {uint64_t(D) * 2, uint64_t(Nq) * D * 2};
   const uint64_t dk_[3] = {uint64_t(D), uint64_t(Nk), uint64_t(B) * Hkv};
   const uint64_t sk[2] = {uint64_t(D) * 2, uint64_t(Nk) * D * 2};
   const uint32_t box64[3] = {64, 64, 1};
+  const bool fused = (D == 128) && dq_acc != nullptr;
   CUtensorMap tk, tv, tdq, tdk, tdv, tq64, tdo64;
   if (!encode_tmap_bf16(&tq64, q, 3, dq_, sq, box64, true, err) ||
       !encode_tmap_bf16(&tdo64, dout, 3, dq_, sq, box64, true, err) ||
-      !encode_tmap_bf16(&tdq, dq, 3, dq_, sq, box, true, err) ||
+      (!fused && !encode_tmap_bf16(&tdq, dq, 3, dq_, sq, box, true, err)) ||
       !encode_tmap_bf16(&tk, k, 3, dk_, sk, box, true, err) ||
       !encode_tmap_bf16(&tv, v, 3, dk_, sk, box, true, err) ||
       !encode_tmap_bf16(&tdk, dk, 3, dk_, sk, box, true, err) ||
       !encode_tmap_bf16(&tdv, dv, 3, dk_, sk, box, true, err))
     return cudaErrorInvalidValue;
-  static thread_local int conf_dq = -1, conf_dkdv = -1;
-  cudaError_t e = set_smem_once(bwd_dq_kernel<D>, DqCfg<D>::kSmemBytes, &conf_dq);
-  if (e != cudaSuccess) return e;
-  e = set_smem_once(bwd_dkdv_kernel<D>, DkvCfg<D>::kSmemBytes, &conf_dkdv);
-  if (e != cudaSuccess) return e;
 
   BArgs a;
   a.q = static_cast<const uint16_t*>(q);
@@ -824,15 +1242,38 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
 
   const long long rows = (long long)B * H * Nq;
   const long long threads = rows * (D / 8);
+  const unsigned grid_kv = unsigned(B) * Hkv * unsigned((Nk + 127) / 128);
+  cudaError_t e;
+  if (fused) {
+    static thread_local int conf_fused = -1;
+    e = set_smem_once(bwd_fused_kernel, FusedCfg::kSmemBytes, &conf_fused);
+    if (e != cudaSuccess) return e;
+    bwd_delta_kernel<D><<<unsigned((threads + 255) / 256), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta, rows, dq_acc);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_fused_kernel<<<grid_kv, 512, FusedCfg::kSmemBytes, stream>>>(tq64, tdo64, tk, tv, tdk, tdv,
+                                                                     a, dq_acc);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long n8 = rows * D / 8;
+    bwd_dq_convert_kernel<<<unsigned((n8 + 255) / 256), 256, 0, stream>>>(
+        dq_acc, static_cast<uint16_t*>(dq), n8, scale);
+    return cudaGetLastError();
+  }
+  static thread_local int conf_dq = -1, conf_dkdv = -1;
+  e = set_smem_once(bwd_dq_kernel<D>, DqCfg<D>::kSmemBytes, &conf_dq);
+  if (e != cudaSuccess) return e;
+  e = set_smem_once(bwd_dkdv_kernel<D>, DkvCfg<D>::kSmemBytes, &conf_dkdv);
+  if (e != cudaSuccess) return e;
   bwd_delta_kernel<D><<<unsigned((threads + 255) / 256), 256, 0, stream>>>(
-      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta, rows);
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta, rows, nullptr);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid_dq = unsigned(B) * H * unsigned((Nq + 127) / 128);
   bwd_dq_kernel<D><<<grid_dq, 384, DqCfg<D>::kSmemBytes, stream>>>(tk, tv, tdq, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const unsigned grid_kv = unsigned(B) * Hkv * unsigned((Nk + 127) / 128);
   bwd_dkdv_kernel<D><<<grid_kv, 384, DkvCfg<D>::kSmemBytes, stream>>>(tq64, tdo64, tk, tv, tdk,
                                                                        tdv, a);
   return cudaGetLastError();
@@ -840,21 +1281,32 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
 
 }  // namespace
 
-size_t backward_workspace_bytes(int B, int H, int Nq) {
+// Workspace: D (B*H*Nq fp32, rounded up to 256 bytes), then, for the fused
+// d = 128 path, the fp32 dQ accumulator [B*H*Nq, 128].
+size_t backward_workspace_bytes(int B, int H, int Nq, int d, bool deterministic) {
   const size_t n = size_t(B) * H * Nq * sizeof(float);
-  return (n + 255) / 256 * 256;
+  const size_t dsz = (n + 255) / 256 * 256;
+  if (deterministic || d != 128) return dsz;
+  return dsz + n * 128;
 }
 
 cudaError_t backward_launch(const void* q, const void* k, const void* v, const void* o,
                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
                             int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
-                            void* workspace, cudaStream_t stream, const char** err) {
+                            bool deterministic, void* workspace, cudaStream_t stream,
+                            const char** err) {
   float* delta = static_cast<float*>(workspace);
-  if (d == 128)
+  if (d == 128) {
+    float* acc = nullptr;
+    if (!deterministic) {
+      const size_t n = size_t(B) * H * Nq * sizeof(float);
+      acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + (n + 255) / 256 * 256);
+    }
     return launch_bwd<128>(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, Nq, Nk, scale, causal,
-                           delta, stream, err);
+                           delta, acc, stream, err);
+  }
   return launch_bwd<64>(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, Nq, Nk, scale, causal, delta,
-                        stream, err);
+                        nullptr, stream, err);
 }
 
 int backward_take_device_error() {

@@ -267,6 +267,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_maj
          | (1u << 10)     // B format: bf16
          | (uint32_t(b_mn_major) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
+// The same with A from shared memory in MN-major order (bit 15): A's M index
+// is the contiguous one, e.g. K^T read from a K tile stored [keys][d].
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_amn(int M, int N, int b_mn_major) {
+  return idesc_bf16_f32(M, N, b_mn_major) | (1u << 15);
+}
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
 // lbo / sbo in bytes (leading / stride byte offsets), version bits = 1.

@@ -464,7 +464,7 @@ def run_ours(args, ws, rank, local):
     # ---- backward pass of the prefill workload (reported beside the step)
     do_ = workloads.grad_output(q_h.shape, seed=rank).to(dev)
     dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    bws = torch.empty(binding.attn_bwd_workspace_size(cfg["B"], cfg["H"], cfg["Nq"]),
+    bws = torch.empty(binding.attn_bwd_workspace_size(cfg["B"], cfg["H"], cfg["Nq"], cfg["d"]),
                       dtype=torch.uint8, device=dev)
     prefill()
 

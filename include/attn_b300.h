@@ -14,7 +14,7 @@
  * - Every tensor is dense and contiguous in the layout stated per call.
  * - Calls are asynchronous on `stream` (NULL = legacy default stream) and
  *   never synchronise.  Results are deterministic: identical calls give
- *   bit-identical outputs.
+ *   bit-identical outputs (except attn_bwd's dq at d = 128, see there).
  * - Errors: on invalid arguments nothing is launched and a non-zero status is
  *   returned; attn_last_error() then returns a human-readable message (per
  *   calling thread).  Kernels bound every internal wait; a wait that times
@@ -143,11 +143,13 @@ ATTN_API attn_status attn_fwd_host(const void* q, const void* k, const void* v, 
                                    size_t workspace_bytes, int chunks, attn_stream_t stream);
 
 /*
- * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs (the
- * per-row fp32 D = rowsum(dO o O), B*H*Nq floats rounded up to 256 bytes).
- * Returns 0 for invalid sizes.  Pure host function.
+ * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs for
+ * these sizes: the per-row fp32 D = rowsum(dO o O) (B*H*Nq floats, rounded
+ * up to 256 bytes) and, for d = 128, an fp32 dQ accumulator of B*H*Nq*128
+ * floats.  Enough for attn_bwd_ex with any flags.  Returns 0 for invalid
+ * sizes.  Pure host function.
  */
-ATTN_API size_t attn_bwd_workspace_size(int B, int H, int Nq);
+ATTN_API size_t attn_bwd_workspace_size(int B, int H, int Nq, int d);
 
 /*
  * attn_bwd -- gradients of attn_fwd: given dO = dL/dO, returns dQ, dK, dV,
@@ -167,10 +169,17 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int H, int Nq);
  *   lse              [B, H,   Nq]     fp32, as written by attn_fwd (natural
  *                    log; -inf for rows with no key)
  *   o                attn_fwd's output for the same q, k, v, scale, causal
- *   workspace        >= attn_bwd_workspace_size(B, H, Nq) bytes, 16-byte
+ *   workspace        >= attn_bwd_workspace_size(B, H, Nq, d) bytes, 16-byte
  *                    aligned, caller-owned; clobbered.
  * Rows with no unmasked key get dq = 0 and contribute nothing to dk, dv.
- * Deterministic: no atomics; identical calls give identical bits.
+ *
+ * At d = 128 one kernel computes all five products per (key tile, query
+ * tile) and adds each key tile's share of dQ into the fp32 accumulator in
+ * the workspace with atomic adds, whose order varies: dq can then differ
+ * between identical calls in the last bits (dk and dv do not).  At d = 64,
+ * and with ATTN_BWD_DETERMINISTIC (attn_bwd_ex), dQ and dK/dV come from two
+ * separate kernels (S and dP computed twice), with no atomics: identical
+ * calls give identical bits.
  *
  * Requirements: as attn_fwd (d in {64, 128}, H % Hkv == 0, pointers 16-byte
  * aligned, lse 4-byte aligned); dq, dk, dv must not alias the inputs.
@@ -180,6 +189,23 @@ ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const
                               int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
                               int causal, void* workspace, size_t workspace_bytes,
                               attn_stream_t stream);
+
+/*
+ * attn_bwd_ex -- attn_bwd with option flags (0 gives exactly attn_bwd).
+ *
+ *   ATTN_BWD_DETERMINISTIC  bit-reproducible results: dQ from a
+ *       query-stationary kernel and dK, dV from a key-stationary one, no
+ *       atomics (the pair recomputes S and dP, seven matrix products instead
+ *       of five, so it is slower).  Needs only the D part of the workspace
+ *       (B*H*Nq floats rounded up to 256 bytes).
+ * Unknown flag bits give ATTN_EINVAL.  Everything else as attn_bwd.
+ */
+#define ATTN_BWD_DETERMINISTIC 1u
+ATTN_API attn_status attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                                 const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                 int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
+                                 int causal, void* workspace, size_t workspace_bytes,
+                                 unsigned flags, attn_stream_t stream);
 
 /*
  * paged_decode_workspace_size -- bytes of device workspace paged_decode needs

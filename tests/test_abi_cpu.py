@@ -31,7 +31,7 @@ def test_header_declares_expected_api():
                                            "attn_fwd_host_workspace_size",
                                            "paged_decode", "paged_decode_workspace_size",
                                            "paged_decode_noalloc", "paged_prefill", "attn_bwd",
-                                           "attn_bwd_workspace_size", "kv_append",
+                                           "attn_bwd_ex", "attn_bwd_workspace_size", "kv_append",
                                            "kv_append_workspace_size", "attn_selftest_wait_timeout",
                                            "attn_last_error",
                                            "attn_device_status"])
@@ -175,9 +175,26 @@ def test_attn_bwd_rejects_bad_arguments(lib, kw, status):
 
 
 def test_bwd_workspace_size(lib):
-    assert lib.attn_bwd_workspace_size(2, 16, 2048) == 2 * 16 * 2048 * 4
-    assert lib.attn_bwd_workspace_size(1, 1, 1) == 256
-    assert lib.attn_bwd_workspace_size(0, 1, 1) == 0
+    # D (rounded up to 256 bytes), plus the fp32 dQ accumulator at d = 128
+    assert lib.attn_bwd_workspace_size(2, 16, 2048, 64) == 2 * 16 * 2048 * 4
+    assert lib.attn_bwd_workspace_size(1, 1, 1, 64) == 256
+    assert lib.attn_bwd_workspace_size(2, 16, 2048, 128) == 2 * 16 * 2048 * 4 * 129
+    assert lib.attn_bwd_workspace_size(1, 1, 1, 128) == 256 + 512
+    assert lib.attn_bwd_workspace_size(0, 1, 1, 128) == 0
+    assert lib.attn_bwd_workspace_size(1, 1, 1, 96) == 0
+
+
+def test_attn_bwd_ex_flags(lib):
+    a = [_fake(i) for i in range(1, 10)]
+    common = (1, 4, 2, 256, 256, 128, 0.088, 1, _fake(10), 1 << 20)
+    # unknown flag bits are rejected before anything else happens
+    assert lib.attn_bwd_ex(*a, *common, 2, None) == binding.ATTN_EINVAL
+    assert "flags" in lib.attn_last_error().decode()
+    # the deterministic path needs only the D part of the workspace; the
+    # default path at d = 128 needs the accumulator too
+    small = (1, 4, 2, 256, 256, 128, 0.088, 1, _fake(10), 4096)
+    assert lib.attn_bwd_ex(*a, *small, 0, None) == binding.ATTN_EINVAL
+    assert "workspace" in lib.attn_last_error().decode()
 
 
 def _app(lib, **kw):
