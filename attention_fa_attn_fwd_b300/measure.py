@@ -1,4 +1,4 @@
-"""L2 flush used between timed kernels (bench.py and profile_cases).
+"""L2 flush used between timed kernels (bench.py and its --case runs).
 
 ``L2Flush()`` writes a 256 MiB buffer (twice the 126 MB L2), which evicts
 every line a timed kernel could reuse, and then reads a second 256 MiB

@@ -99,7 +99,7 @@ def committed_traffic(kernel: str, files):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 20 ms."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -115,7 +115,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -149,6 +149,21 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
                 "samples": len(rows)}
+
+
+def spread(ms):
+    """Mean, median, p10 and p90 (ms) of a list of event times."""
+    xs = sorted(ms)
+    n = len(xs)
+
+    def q(f):
+        i = f * (n - 1)
+        lo = int(math.floor(i))
+        hi = min(n - 1, lo + 1)
+        return xs[lo] + (xs[hi] - xs[lo]) * (i - lo)
+
+    return {"ms_mean": statistics.mean(xs), "ms_median": q(0.5), "ms_p10": q(0.1),
+            "ms_p90": q(0.9), "iters": n}
 
 
 def dist_setup():
@@ -243,6 +258,145 @@ def blas_threads() -> int:
         return os.cpu_count() or 1
 
 
+# ---------------------------------------------------------------- single cases
+# ``--case NAME`` runs one hot-path workload a fixed number of times instead of
+# the benchmark line (the commands of the Nsight Compute summaries under
+# profiles/ use these), or a timing sweep:
+#   prefill        attn_fwd on --prefill (default: the long-context GQA workload)
+#   decode         paged_decode on the 64-sequence workload (--decode-seqs fewer)
+#   step           prefill then decode, as one bench step
+#   paged_prefill  chunked prefill of 8 x 2048 tokens over a paged cache
+#   backward       attn_bwd on --prefill (after one untimed attn_fwd);
+#                  --deterministic selects ATTN_BWD_DETERMINISTIC
+#   sweep          attn_fwd over the length sweep at B*N = 16384 tokens
+#   configs        attn_fwd on each named prefill workload, with and without
+#                  the FMA exp2, and the d64 sweep points with it
+#   decode_sweep   paged_decode of 64 sequences (32 at 16384 tokens) of one
+#                  fixed context length, 512 .. 16384
+# An L2 flush precedes every kernel; each launch's CUDA-event time is printed
+# (sweeps: median of --iters runs and TFLOP/s or GB/s).
+
+def _time(fn, flush, iters: int) -> float:
+    """Median CUDA-event time (ms) of fn over iters runs after 2 warm-ups, each
+    run preceded by an L2 flush outside the events."""
+    for _ in range(2):
+        flush()
+        fn()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    for a, b in evs:
+        flush()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def run_case(args):
+    from attention_fa_attn_fwd_b300 import binding
+    binding.load_library()
+    dev = torch.device("cuda", 0)
+    flush = L2Flush(dev)
+    runs = []
+    if args.case in ("prefill", "step"):
+        cfg = dict(workloads.PREFILL_WORKLOADS.get(args.prefill) or workloads.sweep_workloads()[args.prefill])
+        q, k, v = (t.to(dev) for t in workloads.prefill_inputs(**cfg))
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        runs.append(("attn_fwd", lambda: binding.attn_fwd(q, k, v, causal=cfg["causal"], o=o, lse=lse)))
+    if args.case in ("decode", "step"):
+        dcfg = dict(workloads.PAGED_WORKLOADS["paged_decode_s64_h32kv8_d128"])
+        dcfg["num_seqs"] = args.decode_seqs
+        pb = workloads.paged_decode_inputs(**dcfg)
+        dq, kc, vc = pb.q.to(dev), pb.k_cache.to(dev), pb.v_cache.to(dev)
+        bt, sl = pb.block_table.to(dev), pb.seq_lens.to(dev)
+        do = torch.empty_like(dq)
+        dl = torch.empty(dq.shape[:2], dtype=torch.float32, device=dev)
+        n = binding.paged_decode_workspace_size(dq.shape[0], dq.shape[1], kc.shape[1], dq.shape[2],
+                                                bt.shape[1])
+        ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        runs.append(("paged_decode", lambda: binding.paged_decode(dq, kc, vc, bt, sl, o=do, lse=dl,
+                                                                  workspace=ws)))
+    if args.case == "paged_prefill":
+        pcfg = workloads.PAGED_PREFILL_WORKLOADS["paged_prefill_s8_h32kv8_q2048_d128"]
+        pp = workloads.paged_prefill_inputs(**pcfg)
+        pq, pkc, pvc = pp.q.to(dev), pp.k_cache.to(dev), pp.v_cache.to(dev)
+        pbt, psl = pp.block_table.to(dev), pp.seq_lens.to(dev)
+        po = torch.empty_like(pq)
+        pl = torch.empty(pq.shape[:3], dtype=torch.float32, device=dev)
+        runs.append(("paged_prefill", lambda: binding.paged_prefill(pq, pkc, pvc, pbt, psl,
+                                                                    o=po, lse=pl)))
+    if args.case == "backward":
+        cfg = dict(workloads.PREFILL_WORKLOADS.get(args.prefill) or workloads.sweep_workloads()[args.prefill])
+        q, k, v = (t.to(dev) for t in workloads.prefill_inputs(**cfg))
+        do = workloads.grad_output(q.shape).to(dev)
+        o, lse = binding.attn_fwd(q, k, v, causal=cfg["causal"])
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bws = torch.empty(binding.attn_bwd_workspace_size(*q.shape[:3], q.shape[3]),
+                          dtype=torch.uint8, device=dev)
+        runs.append(("attn_bwd", lambda: binding.attn_bwd(q, k, v, o, do, lse, causal=cfg["causal"],
+                                                          dq=dq, dk=dk, dv=dv, workspace=bws,
+                                                          deterministic=args.deterministic)))
+    if args.case == "configs":
+        todo = [(n, c, False) for n, c in workloads.PREFILL_WORKLOADS.items()]
+        todo += [(n, c, True) for n, c in workloads.PREFILL_WORKLOADS.items()]
+        todo += [(n, c, True) for n, c in workloads.sweep_workloads().items() if c["d"] == 64]
+        for name, cfg, fma in todo:
+            q, k, v = (t.to(dev) for t in workloads.prefill_inputs(**cfg))
+            o = torch.empty_like(q)
+            lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+            ms = _time(lambda: binding.attn_fwd(q, k, v, causal=cfg["causal"], o=o, lse=lse,
+                                                exp2_fma=fma), flush, args.iters)
+            fl = 4.0 * cfg["B"] * cfg["H"] * cfg["Nq"] * cfg["Nk"] * cfg["d"]
+            fl = fl / 2 if cfg["causal"] else fl
+            tag = " exp2_fma" if fma else ""
+            print(f"{name}{tag}: {ms:.4f} ms  {fl / ms / 1e9:.1f} TFLOP/s", flush=True)
+            del q, k, v, o, lse
+        return
+    if args.case == "sweep":
+        for name, cfg in workloads.sweep_workloads().items():
+            q, k, v = (t.to(dev) for t in workloads.prefill_inputs(**cfg))
+            o = torch.empty_like(q)
+            lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+            ms = _time(lambda: binding.attn_fwd(q, k, v, causal=cfg["causal"], o=o, lse=lse),
+                       flush, args.iters)
+            fl = 4.0 * cfg["B"] * cfg["H"] * cfg["Nq"] * cfg["Nk"] * cfg["d"]
+            fl = fl / 2 if cfg["causal"] else fl
+            print(f"{name}: {ms:.4f} ms  {fl / ms / 1e9:.1f} TFLOP/s", flush=True)
+            del q, k, v, o, lse
+        return
+    if args.case == "decode_sweep":
+        for L in (512, 1024, 2048, 4096, 8192, 16384):
+            S = min(64, 64 * 8192 // L)
+            pb = workloads.paged_decode_inputs(num_seqs=S, H=32, Hkv=8, d=128, min_len=L,
+                                               max_len=L, group=1, shared_tokens=0, seed=0)
+            dq, kc, vc = pb.q.to(dev), pb.k_cache.to(dev), pb.v_cache.to(dev)
+            bt, sl = pb.block_table.to(dev), pb.seq_lens.to(dev)
+            do = torch.empty_like(dq)
+            dl = torch.empty(dq.shape[:2], dtype=torch.float32, device=dev)
+            n = binding.paged_decode_workspace_size(S, 32, 8, 128, bt.shape[1])
+            ws = torch.empty(n, dtype=torch.uint8, device=dev)
+            ms = _time(lambda: binding.paged_decode(dq, kc, vc, bt, sl, o=do, lse=dl, workspace=ws),
+                       flush, args.iters)
+            nbytes = pb.unique_valid_tokens() * 8 * 128 * 2 * 2
+            print(f"decode_s{S}_len{L}: {ms * 1e3:.1f} us  {nbytes / ms / 1e6:.1f} GB/s", flush=True)
+            del dq, kc, vc, bt, sl, do, dl, ws
+        return
+    for it in range(args.iters):
+        for name, fn in runs:
+            flush()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            print(f"{name} iter {it}: {a.elapsed_time(b):.3f} ms", flush=True)
+    assert binding.device_status() == 0
+
+
+
 # ---------------------------------------------------------------- arms
 
 def run_reference(args, ws, rank):
@@ -262,15 +416,17 @@ def run_reference(args, ws, rank):
         vals.append(tf)
         dec.append(gbs)
         secs.append(t + td)
-    value = statistics.median(vals)
+    value = statistics.mean(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
+        "ms_per_step": 1e3 * statistics.mean(secs), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{PREFILL} + {DECODE}", "prefill": cfg,
-                   "decode": workloads.PAGED_WORKLOADS[DECODE], "l2": "n/a (CPU)"},
-        "decode": {"value": statistics.median(dec), "unit": "GB/s"},
+                   "decode": workloads.PAGED_WORKLOADS[DECODE]},
+        "timing": {"l2": "n/a (CPU)", "parallelism": "rank 0 only", "aggregate": "mean",
+                   "step_s": spread([1e3 * x for x in secs])},
+        "decode": {"value": statistics.mean(dec), "unit": "GB/s"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
                          "kind": "oracle", "sample": f"per step: {desc}; decode {ddesc}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -343,6 +499,7 @@ def run_ours(args, ws, rank, local):
     d_ms = [evs[i][2].elapsed_time(evs[i][3]) for i in range(K)]
     p_mean = max_over_ranks(statistics.mean(p_ms), ws)
     d_mean = max_over_ranks(statistics.mean(d_ms), ws)
+    p_spread, d_spread = spread(p_ms), spread(d_ms)
     assert binding.device_status(stream) == 0
 
     # Whole-job throughput: every rank ran the same step (independent replicas),
@@ -468,25 +625,31 @@ def run_ours(args, ws, rank, local):
                       dtype=torch.uint8, device=dev)
     prefill()
 
-    def backward():
-        binding.attn_bwd(q, k, v, o, do_, lse, causal=True, dq=dq_, dk=dk_, dv=dv_,
-                         workspace=bws, stream=stream)
+    def time_backward(det: bool):
+        def backward():
+            binding.attn_bwd(q, k, v, o, do_, lse, causal=True, dq=dq_, dk=dk_, dv=dv_,
+                             workspace=bws, stream=stream, deterministic=det)
 
-    for _ in range(3):
-        flush()
-        backward()
-    Kb = max(3, min(K, 50))
-    b_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kb)]
-    for i in range(Kb):
-        flush()
-        b_evs[i][0].record(stream)
-        backward()
-        b_evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    assert binding.device_status(stream) == 0
-    bw_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in b_evs), ws)
+        for _ in range(3):
+            flush()
+            backward()
+        Kb = max(3, min(K, 50))
+        b_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kb)]
+        for i in range(Kb):
+            flush()
+            b_evs[i][0].record(stream)
+            backward()
+            b_evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        assert binding.device_status(stream) == 0
+        ms = [e[0].elapsed_time(e[1]) for e in b_evs]
+        return max_over_ranks(statistics.mean(ms), ws), spread(ms)
+
+    bw_ms, bw_spread = time_backward(False)
+    bwd_ms, bwd_spread = time_backward(True)
     bw_flops = 2.5 * prefill_flops(cfg) * ws  # 5 matrix products vs the forward's 2
     bw_tflops = bw_flops / (bw_ms * 1e-3) / 1e12
+    bwd_tflops = bw_flops / (bwd_ms * 1e-3) / 1e12
     del do_, dq_, dk_, dv_, bws
 
     # ---- end to end through the public API with pinned host buffers
@@ -545,13 +708,15 @@ def run_ours(args, ws, rank, local):
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": p_mean + d_mean, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{PREFILL} + {DECODE}", "prefill": cfg, "decode": dcfg,
-                   "l2": "L2 flush before every timed kernel, outside the events: write 256 MiB, "
+        "config": {"workload": f"{PREFILL} + {DECODE}", "prefill": cfg, "decode": dcfg},
+        "timing": {"l2": "L2 flush before every timed kernel, outside the events: write 256 MiB, "
                          "then read 256 MiB (clean lines)",
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "aggregate": "mean of the K event times (rank 0's spread beside it)"},
         "prefill": {"ms": p_mean, "tflops": tflops, "frac_burst": k_tflops / peak_tf,
-                    "frac_sustained": k_tflops / peaks["bf16_tflops_sustained"]},
-        "decode": {"ms": d_mean, "value": dec_gbs, "unit": "GB/s",
+                    "frac_sustained": k_tflops / peaks["bf16_tflops_sustained"], **p_spread,
+                    "tflops_median": flops / ws / (p_spread["ms_median"] * 1e-3) / 1e12},
+        "decode": {"ms": d_mean, "value": dec_gbs, "unit": "GB/s", **d_spread,
                    "unique_kv_bytes": uniq_bytes, "logical_kv_bytes": logical_bytes,
                    "logical_gbs": ws * (logical_bytes + small_bytes) / (d_mean * 1e-3) / 1e9,
                    "frac_hbm_measured": k_gbs / peaks["hbm_gbs"], "frac_hbm_8tbs": k_gbs / 8000.0},
@@ -575,9 +740,13 @@ def run_ours(args, ws, rank, local):
                       "note": f"CUDA graph of {APPEND_STEPS} decode-step appends, time / steps; "
                               "latency-bound: 2 launches, 262 KB of new K/V rows per step"},
         "backward": {"workload": PREFILL, "ms": bw_ms, "tflops": bw_tflops,
-                     "frac_burst": bw_tflops / ws / peak_tf,
+                     "frac_burst": bw_tflops / ws / peak_tf, **bw_spread,
                      "flops": bw_flops / ws, "flops_note": "algorithmic: 2.5 x forward (5 products)",
-                     "kernels": "bwd_delta_kernel + bwd_dq_kernel<128> + bwd_dkdv_kernel<128>"},
+                     "kernels": "bwd_delta_kernel + bwd_fused_kernel + bwd_dq_convert_kernel"},
+        "backward_deterministic": {"workload": PREFILL, "ms": bwd_ms, "tflops": bwd_tflops,
+                                   "frac_burst": bwd_tflops / ws / peak_tf, **bwd_spread,
+                                   "kernels": "bwd_delta_kernel + bwd_dq_kernel<128> + "
+                                              "bwd_dkdv_kernel<128> (ATTN_BWD_DETERMINISTIC)"},
         "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "prefill_ms": ep, "decode_ms": ed,
                 "path": "prefill: attn_fwd_host on pinned host buffers (copies overlapped with "
@@ -600,9 +769,21 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of CPU oracle work for the cpu_baseline")
+    ap.add_argument("--case", choices=["prefill", "decode", "step", "paged_prefill", "backward",
+                                       "sweep", "decode_sweep", "configs"], default=None,
+                    help="run one workload (for Nsight Compute) or a sweep instead of the bench line")
+    ap.add_argument("--iters", type=int, default=3, help="--case: runs per workload")
+    ap.add_argument("--prefill", default=PREFILL, help="--case prefill/backward: workload name")
+    ap.add_argument("--decode-seqs", type=int, default=64,
+                    help="--case decode/step: sequences of the decode workload")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="--case backward: ATTN_BWD_DETERMINISTIC")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.case:
+        run_case(args)
+        return
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, ws, rank)
