@@ -25,7 +25,8 @@ ATTN_EINVAL = 1
 ATTN_EUNSUPPORTED = 2
 ATTN_ECUDA = 3
 ATTN_EDEVICE = 4
-ATTN_FWD_EXP2_FMA = 1  # attn_fwd_ex flag
+ATTN_FWD_EXP2_FMA = 1  # attn_fwd_ex flags
+ATTN_FWD_DIAG_WAIT_EXPIRES = 2
 ATTN_BWD_DETERMINISTIC = 1  # attn_bwd_ex flag
 _STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_EINVAL", 2: "ATTN_EUNSUPPORTED",
                  3: "ATTN_ECUDA", 4: "ATTN_EDEVICE"}
@@ -119,12 +120,15 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
              causal: bool = False, scale: Optional[float] = None,
              o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
              want_lse: bool = True, stream=None,
-             exp2_fma: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+             exp2_fma: bool = False,
+             diag_wait_expires: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """O = softmax(scale Q K^T [causal]) V and per-row LSE via ``attn_fwd``.
 
     q [B,H,Nq,d], k/v [B,Hkv,Nk,d], bf16, contiguous, on one CUDA device.
     Returns (o [B,H,Nq,d] bf16, lse [B,H,Nq] fp32 or None).
-    ``exp2_fma=True`` calls ``attn_fwd_ex`` with ATTN_FWD_EXP2_FMA.
+    ``exp2_fma=True`` calls ``attn_fwd_ex`` with ATTN_FWD_EXP2_FMA;
+    ``diag_wait_expires=True`` adds ATTN_FWD_DIAG_WAIT_EXPIRES (a
+    failure-detection test: the outputs are then undefined).
     """
     lib = load_library()
     _need(q, "q", torch.bfloat16, 4)
@@ -148,11 +152,13 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         _need(lse, "lse", torch.float32, 3)
         if tuple(lse.shape) != (B, H, Nq):
             raise ValueError("lse must be [B, H, Nq]")
-    if exp2_fma:
+    flags = (ATTN_FWD_EXP2_FMA if exp2_fma else 0) | \
+        (ATTN_FWD_DIAG_WAIT_EXPIRES if diag_wait_expires else 0)
+    if flags:
         st = lib.attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                              lse.data_ptr() if lse is not None else None,
                              B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
-                             ATTN_FWD_EXP2_FMA, _stream_handle(stream))
+                             flags, _stream_handle(stream))
     else:
         st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                           lse.data_ptr() if lse is not None else None,

@@ -2,6 +2,7 @@
 // validation, device check, TMA descriptor encoding, kernel dispatch.
 // Nothing is launched on invalid input.
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -103,6 +104,13 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64
   return true;
 }
 
+unsigned next_launch_id() {
+  static std::atomic<unsigned> seq{0};
+  unsigned id = seq.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (id == 0) id = seq.fetch_add(1, std::memory_order_relaxed) + 1;  // skip 0 on wrap
+  return id;
+}
+
 void set_last_error(const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -127,7 +135,8 @@ attn_status attn_fwd_ex(const void* q, const void* k, const void* v, void* o, fl
   if (!(scale > 0.f) || !(scale < 3.0e38f))
     return fail(ATTN_EINVAL, "attn_fwd: scale must be positive and finite");
   if (causal != 0 && causal != 1) return fail(ATTN_EINVAL, "attn_fwd: causal must be 0 or 1");
-  if (flags & ~unsigned(ATTN_FWD_EXP2_FMA)) return fail(ATTN_EINVAL, "attn_fwd: unknown flags 0x%x", flags);
+  if (flags & ~unsigned(ATTN_FWD_EXP2_FMA | ATTN_FWD_DIAG_WAIT_EXPIRES))
+    return fail(ATTN_EINVAL, "attn_fwd: unknown flags 0x%x", flags);
   if (d != 64 && d != 128) return fail(ATTN_EUNSUPPORTED, "attn_fwd: head dim %d (need 64 or 128)", d);
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       (lse && !aligned(lse, 4)))
@@ -137,8 +146,10 @@ attn_status attn_fwd_ex(const void* q, const void* k, const void* v, void* o, fl
   attn_status st = check_device();
   if (st != ATTN_OK) return st;
   const char* err = nullptr;
+  // The diagnostic wait's limit: 1 ms.
+  const unsigned diag_ns = (flags & ATTN_FWD_DIAG_WAIT_EXPIRES) ? 1000000u : 0u;
   cudaError_t e = attn::prefill_launch(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal,
-                                       (flags & ATTN_FWD_EXP2_FMA) != 0,
+                                       (flags & ATTN_FWD_EXP2_FMA) != 0, diag_ns,
                                        reinterpret_cast<cudaStream_t>(stream), &err);
   if (err) return fail(ATTN_ECUDA, "attn_fwd: %s", err);
   if (e != cudaSuccess) return fail(ATTN_ECUDA, "attn_fwd launch: %s", cudaGetErrorString(e));

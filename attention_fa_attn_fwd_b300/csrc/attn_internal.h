@@ -16,7 +16,8 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64
 // ---- prefill (prefill_sm103.cu)
 cudaError_t prefill_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                            int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
-                           bool poly_exp, cudaStream_t stream, const char** err);
+                           bool poly_exp, unsigned diag_wait_ns, cudaStream_t stream,
+                           const char** err);
 cudaError_t paged_prefill_launch(const void* q, const void* k_cache, const void* v_cache,
                                  const int32_t* block_table, const int32_t* kv_lens, int B, int H,
                                  int Hkv, int Nq, int d, int num_blocks, int max_blocks,
@@ -66,5 +67,10 @@ int append_take_device_error();
 
 // Sets the calling thread's attn_last_error() message (printf-style).
 void set_last_error(const char* fmt, ...);
+
+// A fresh id for one kernel launch (process-wide counter, never 0): a kernel
+// whose bounded wait expires records it, and only CTAs of that same launch
+// skip their work because of it.
+unsigned next_launch_id();
 
 }  // namespace attn

@@ -46,7 +46,7 @@
 
 namespace attn {
 
-__device__ int g_backward_error;
+__device__ int g_backward_error[2];  // see ErrSink
 
 namespace {
 
@@ -103,6 +103,7 @@ struct BArgs {
   float c_log2;  // scale * log2(e)
   float scale;
   int causal;
+  unsigned launch_id;  // set per kernel launch (see ErrSink)
 };
 
 // -log2-domain LSE: P = 2^(s * c_log2 + neg_lse2).  A row with no key
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(384, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
-  int* err = &g_backward_error;
+  const ErrSink err{g_backward_error, a.launch_id};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // Heavy (late, causal) query tiles first; heads of one KV group adjacent.
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(384, 1)
   const int q0 = (n_qt - 1 - int(blockIdx.x / BH)) * 128;
   const int b = bh / a.H, h = bh % a.H;
   const int zkv = b * a.Hkv + h / (a.H / a.Hkv);
-  const bool dead = timed_out_before(err);
+  const bool dead = err.this_launch_timed_out();
   int kv_end = a.Nk;
   if (a.causal) kv_end = min(a.Nk, q0 + 128 + (a.Nk - a.Nq));
   const int n = (kv_end > 0 && !dead) ? (kv_end + 127) / 128 : 0;
@@ -492,7 +493,7 @@ __global__ void __launch_bounds__(384, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   float* stat = reinterpret_cast<float*>(smem + C::kOffStat);
-  int* err = &g_backward_error;
+  const ErrSink err{g_backward_error, a.launch_id};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // CTA = (b, KV head, KV tile), KV tiles of one head adjacent so resident
@@ -510,7 +511,7 @@ __global__ void __launch_bounds__(384, 1)
     const int first_row = k0 - off;  // first query row that sees key k0
     qt0 = first_row <= 0 ? 0 : first_row / 128;
   }
-  const bool dead = timed_out_before(err);
+  const bool dead = err.this_launch_timed_out();
   const int per_head = max(0, n_qt - qt0);
   const int n_it = dead ? 0 : G * per_head;  // (query head, query tile) pairs
 
@@ -842,7 +843,7 @@ __global__ void __launch_bounds__(512, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   float* stat = reinterpret_cast<float*>(smem + C::kOffStat);
-  int* err = &g_backward_error;
+  const ErrSink err{g_backward_error, a.launch_id};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // CTA = (b, KV head, key tile); key tiles of one head adjacent (L2 reuse of
@@ -859,7 +860,7 @@ __global__ void __launch_bounds__(512, 1)
     const int first_row = k0 - off;
     qt0 = first_row <= 0 ? 0 : first_row / 128;
   }
-  const bool dead = timed_out_before(err);
+  const bool dead = err.this_launch_timed_out();
   const int per_head = max(0, n_qt - qt0);
   const int n_it = dead ? 0 : G * per_head;
 
@@ -1254,6 +1255,7 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
         static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta, rows, dq_acc);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    a.launch_id = next_launch_id();
     bwd_fused_kernel<<<grid_kv, 512, FusedCfg::kSmemBytes, stream>>>(tq64, tdo64, tk, tv, tdk, tdv,
                                                                      a, dq_acc);
     e = cudaGetLastError();
@@ -1273,9 +1275,11 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid_dq = unsigned(B) * H * unsigned((Nq + 127) / 128);
+  a.launch_id = next_launch_id();
   bwd_dq_kernel<D><<<grid_dq, 384, DqCfg<D>::kSmemBytes, stream>>>(tk, tv, tdq, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  a.launch_id = next_launch_id();
   bwd_dkdv_kernel<D><<<grid_kv, 384, DkvCfg<D>::kSmemBytes, stream>>>(tq64, tdo64, tk, tv, tdk,
                                                                        tdv, a);
   return cudaGetLastError();

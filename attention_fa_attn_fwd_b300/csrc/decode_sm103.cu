@@ -31,7 +31,7 @@
 
 namespace attn {
 
-__device__ int g_decode_error;
+__device__ int g_decode_error[2];  // see ErrSink
 
 namespace {
 
@@ -61,6 +61,7 @@ struct DArgs {
   float* ws_ml;            // [S, H, max_splits, 2]  (m, l) in log2 units
   int H, Hkv, G, num_blocks, max_blocks, bps, max_splits;
   float c_log2;
+  unsigned launch_id;  // set per kernel launch (see ErrSink)
 };
 
 __device__ __forceinline__ void mma_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(128)
   uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + kWarps * kRing * 8);
-  int* err = &g_decode_error;
+  const ErrSink err{g_decode_error, a.launch_id};
 
   // The merge kernel may be scheduled once every CTA of this grid has
   // started; it waits for this grid's completion before reading partials.
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(128)
   const int nblk = min((max(seq_len, 0) + kBlockTokens - 1) / kBlockTokens, a.max_blocks);
   const int b_lo = r * a.bps;
   if (b_lo >= nblk) return;  // split past the end of this sequence: no partial
-  if (timed_out_before(err)) return;  // partial left unwritten; error already recorded
+  if (err.this_launch_timed_out()) return;  // partial left unwritten; error already recorded
   const int b_hi = min(nblk, b_lo + a.bps);
 
   auto bar = [&](int w, int st) -> uint32_t { return sbase + C::kOffBar + 8u * (w * kRing + st); };
@@ -155,12 +156,12 @@ __global__ void __launch_bounds__(128)
   if (lane < n_mine) {
     my_phys = bt[b_lo + warp + kWarps * lane];
     if (my_phys < 0 || my_phys >= a.num_blocks) {
-      atomicCAS(err, 0, kErrDecodeBadBlock);
+      err.record(kErrDecodeBadBlock);
       my_phys = a.num_blocks;  // outside the tensor map: TMA fills zeros
     }
   }
   if (r == 0 && g == 0 && threadIdx.x == 0 && seq_len > a.max_blocks * kBlockTokens)
-    atomicCAS(err, 0, kErrDecodeBadBlock);
+    err.record(kErrDecodeBadBlock);
   auto issue = [&](int i, int phys) {  // lane 0: TMA-load the i-th block of this warp
     const int st = i % kRing;
     const uint32_t dst = wbase + st * C::kStageBytes;
@@ -425,6 +426,7 @@ cudaError_t launch(const void* q, const void* k_cache, const void* v_cache, cons
   a.max_splits = plan.max_splits;
   a.c_log2 = scale * kLog2e;
   dim3 grid(plan.max_splits, Hkv, S);
+  a.launch_id = next_launch_id();
   decode_split_kernel<D><<<grid, 128, C::kSmemBytes, stream>>>(tk, tv, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

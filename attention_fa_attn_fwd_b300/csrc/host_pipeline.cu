@@ -155,7 +155,7 @@ cudaError_t fwd_host_launch(const void* q_h, const void* k_h, const void* v_h, v
     if ((e = cudaStreamWaitEvent(stream, p->loaded[c], 0)) != cudaSuccess) return fail_joined(e);
     e = prefill_launch(dq + u0 * q_unit, dk + u0 * kv_unit, dv + u0 * kv_unit, dout + u0 * q_unit,
                        lse_h ? dlse + u0 * lse_unit : nullptr, 1, n * G, n, Nq, Nk, d, scale,
-                       causal, false, stream, err);
+                       causal, false, 0u, stream, err);
     if (e != cudaSuccess || (err && *err))
       return fail_joined(e != cudaSuccess ? e : cudaErrorInvalidValue);
     if ((e = cudaEventRecord(p->computed[c], stream)) != cudaSuccess ||

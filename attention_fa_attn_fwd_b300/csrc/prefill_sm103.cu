@@ -54,7 +54,7 @@
 
 namespace attn {
 
-__device__ int g_prefill_error;
+__device__ int g_prefill_error[2];  // see ErrSink
 
 namespace {
 
@@ -90,7 +90,8 @@ struct Cfg {
   static constexpr int kBarPF2 = kBarPF + 2;          // 2: P_i keys 64..127 written
   static constexpr int kBarOF = kBarPF2 + 2;          // 2: last PV of tile i done
   static constexpr int kBarDrain = kBarOF + 2;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarDiag = kBarDrain + 1;      // never signalled (diagnostic wait)
+  static constexpr int kNumBars = kBarDiag + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-B alignment
   static constexpr uint32_t kTmemCols = 512;
@@ -115,6 +116,8 @@ struct Args {
   int max_blocks, num_blocks;
   int oob_row;                 // a pool row past the end: TMA fills zeros
   int group_major;             // CTA order (see the kernel)
+  unsigned launch_id;          // set per kernel launch (see ErrSink)
+  unsigned diag_wait_ns;       // != 0: CTA 0 lets one bounded wait expire (failure test)
 };
 
 constexpr int kPageTokens = 16;  // PagedAttention block size
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(384, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
-  int* err = &g_prefill_error;
+  const ErrSink err{g_prefill_error, a.launch_id};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -210,7 +213,7 @@ __global__ void __launch_bounds__(384, 1)
   const int h = bh % a.H;
   const int g_kv = h / (a.H / a.Hkv);
   const int zkv = b * a.Hkv + g_kv;
-  const bool dead = timed_out_before(err);
+  const bool dead = err.this_launch_timed_out();
   // Keys of this sequence; the paged variant reads its own length.
   int Nk = a.Nk;
   int nblk = 0;  // paged: cached blocks of this sequence
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(384, 1)
     Nk = a.kv_lens[b];
     if (Nk < 0 || Nk > a.max_blocks * kPageTokens) {
       if (threadIdx.x == 0 && q0 == (a.n_pairs - 1) * 256 && h == 0)
-        atomicCAS(err, 0, kErrPagedBadLength);
+        err.record(kErrPagedBadLength);
       Nk = min(max(Nk, 0), a.max_blocks * kPageTokens);
     }
     nblk = (Nk + kPageTokens - 1) / kPageTokens;
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(384, 1)
     if (a.causal) kv_end = min(Nk, r0 + 128 + (Nk - a.Nq));
     n_t[i] = (r0 < a.Nq && kv_end > 0 && !dead) ? (kv_end + 127) / 128 : 0;
   }
-  const int n_kv = max(n_t[0], n_t[1]);
+  int n_kv = max(n_t[0], n_t[1]);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) {
@@ -257,6 +260,19 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // Failure-detection test (attn_fwd_ex with ATTN_FWD_DIAG_WAIT_EXPIRES): in
+  // CTA 0, before any copy or MMA is issued, one thread waits on a barrier
+  // nothing signals, with a short limit.  The wait expires and records a
+  // timeout for this launch; the CTA then does no work, and later CTAs of the
+  // same launch skip theirs.  Other launches are unaffected.
+  if (a.diag_wait_ns != 0 && blockIdx.x == 0) {
+    if (threadIdx.x == 0)
+      mbar_wait_limit(bar(C::kBarDiag), 0, abort_flag, err, kErrTimeoutDiag, a.diag_wait_ns);
+    __syncthreads();
+    n_t[0] = n_t[1] = 0;
+    n_kv = 0;
+  }
 
   if (warp < 4) {
     setmaxnreg_dec<C::kRegsLow>();
@@ -305,7 +321,7 @@ __global__ void __launch_bounds__(384, 1)
                 if (phys >= 0 && phys < a.num_blocks)
                   prow = (phys * a.Hkv + g_kv) * kPageTokens;
                 else
-                  atomicCAS(err, 0, kErrPagedBadBlock);
+                  err.record(kErrPagedBadBlock);
               }
             }
             return prow;
@@ -371,7 +387,7 @@ __global__ void __launch_bounds__(384, 1)
                 if (phys >= 0 && phys < a.num_blocks)
                   prow = (phys * a.Hkv + g_kv) * kPageTokens;
                 else
-                  atomicCAS(err, 0, kErrPagedBadBlock);
+                  err.record(kErrPagedBadBlock);
               }
             }
             ok = __all_sync(0xffffffffu,
@@ -721,8 +737,8 @@ bool encode_q_o(CUtensorMap* tq, CUtensorMap* to, const void* q, void* o, int B,
 
 template <int D, bool kPolyExp>
 cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                   int Hkv, int Nq, int Nk, float scale, int causal, cudaStream_t stream,
-                   const char** err) {
+                   int Hkv, int Nq, int Nk, float scale, int causal, unsigned diag_wait_ns,
+                   cudaStream_t stream, const char** err) {
   using C = Cfg<D>;
   CUtensorMap tq, tk, tv, to;
   const uint32_t box[3] = {64, 128, 1};
@@ -745,6 +761,8 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
   a.causal = causal;
   // K + V of every group at once above ~96 MB would thrash the 126 MB L2.
   a.group_major = (uint64_t(B) * Hkv * Nk * D * 4 > (96ull << 20)) ? 1 : 0;
+  a.diag_wait_ns = diag_wait_ns;
+  a.launch_id = next_launch_id();
   const unsigned grid = unsigned(a.n_pairs) * unsigned(B) * unsigned(H);
   prefill_fwd_kernel<D, false, kPolyExp><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv,
                                                                                      to, a);
@@ -785,6 +803,7 @@ cudaError_t launch_paged(const void* q, const void* k_cache, const void* v_cache
   a.num_blocks = num_blocks;
   a.oob_row = int(rows);
   a.group_major = 1;  // sequences have their own caches: keep one group's in L2
+  a.launch_id = next_launch_id();
   const unsigned grid = unsigned(a.n_pairs) * unsigned(B) * unsigned(H);
   prefill_fwd_kernel<D, true, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
@@ -794,15 +813,17 @@ cudaError_t launch_paged(const void* q, const void* k_cache, const void* v_cache
 
 cudaError_t prefill_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                            int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
-                           bool poly_exp, cudaStream_t stream, const char** err) {
+                           bool poly_exp, unsigned diag_wait_ns, cudaStream_t stream,
+                           const char** err) {
+  const unsigned w = diag_wait_ns;
   if (poly_exp) {
     if (d == 128)
-      return launch<128, true>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, stream, err);
-    return launch<64, true>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, stream, err);
+      return launch<128, true>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, w, stream, err);
+    return launch<64, true>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, w, stream, err);
   }
   if (d == 128)
-    return launch<128, false>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, stream, err);
-  return launch<64, false>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, stream, err);
+    return launch<128, false>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, w, stream, err);
+  return launch<64, false>(q, k, v, o, lse, B, H, Hkv, Nq, Nk, scale, causal, w, stream, err);
 }
 
 cudaError_t paged_prefill_launch(const void* q, const void* k_cache, const void* v_cache,

@@ -20,6 +20,7 @@ enum : int {
   kErrTimeoutMma = 0x102,
   kErrTimeoutSoftmax = 0x103,
   kErrTimeoutEpilogue = 0x104,
+  kErrTimeoutDiag = 0x105,      // the deliberate wait of ATTN_FWD_DIAG_WAIT_EXPIRES
   kErrTimeoutSelftest = 0x1FF,  // the deliberate wait of attn_selftest_wait_timeout
   kErrDecodeBadBlock = 0x201,
   kErrPagedBadBlock = 0x202,   // paged prefill: block id outside [0, num_blocks)
@@ -27,6 +28,28 @@ enum : int {
   kErrAppendTable = 0x301,     // kv_append: length < 0 or the table is full
   kErrAppendBlock = 0x302,     // kv_append: a table entry is not a block id
   kErrAppendNoFree = 0x303,    // kv_append: not enough free blocks
+};
+
+// Where a kernel reports errors.  word[0] holds the first error code any launch
+// recorded (kept until attn_device_status reads and clears it); word[1] holds
+// the id of the last launch in which a bounded wait expired.  Every launch
+// gets a fresh id from the host (never 0), so the skip below stays inside the
+// launch that timed out: later launches, and launches running at the same
+// time on other streams, do their full work.
+struct ErrSink {
+  int* word;
+  unsigned launch;
+  __device__ __forceinline__ void record(int code) const { atomicCAS(word, 0, code); }
+  __device__ __forceinline__ void record_timeout(int code) const {
+    atomicCAS(word, 0, code);
+    atomicExch(reinterpret_cast<unsigned*>(word) + 1, launch);
+  }
+  // True if a wait of this same launch has already timed out: its later CTAs
+  // then skip their work, so one systematic failure costs one timeout, not
+  // one per CTA.
+  __device__ __forceinline__ bool this_launch_timed_out() const {
+    return reinterpret_cast<const volatile unsigned*>(word)[1] == launch;
+  }
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -67,11 +90,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait until the phase of `bar` with parity `parity` has completed.
 // Returns false (without completing) if `abort_flag` is raised by another
-// thread, or after kWaitTimeoutNs, in which case it raises the flag itself and
-// records `code` in *err.
+// thread, or after limit_ns, in which case it raises the flag itself and
+// records `code` (and this launch) in err.
 __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity,
-                                                volatile int* abort_flag, int* err, int code,
-                                                uint64_t limit_ns) {
+                                                volatile int* abort_flag, const ErrSink& err,
+                                                int code, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
@@ -80,14 +103,14 @@ __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity,
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
-        if (err) atomicCAS(err, 0, code);
+        err.record_timeout(code);
         return false;
       }
     }
   }
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err, int code) {
+                                          const ErrSink& err, int code) {
   return mbar_wait_limit(bar, parity, abort_flag, err, code, kWaitTimeoutNs);
 }
 
@@ -98,13 +121,6 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
     if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() > deadline) return false;
   }
-}
-
-// True if an earlier CTA of this library already timed out: later CTAs then
-// skip their work, so one systematic failure costs one timeout, not one per CTA.
-__device__ __forceinline__ bool timed_out_before(const int* err) {
-  const int e = *reinterpret_cast<const volatile int*>(err);
-  return (e & 0xF00) == 0x100;
 }
 
 // ------------------------------------------------------------------ TMA

@@ -16,7 +16,7 @@
 
 namespace attn {
 
-__device__ int g_selftest_error;
+__device__ int g_selftest_error[2];  // see ErrSink
 
 namespace {
 
@@ -31,9 +31,9 @@ __global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(uint64_t limi
   }
   __syncwarp();
   // Nothing arrives on `bar`: this wait must give up after limit_ns.
-  const bool ok = mbar_wait_limit(bar, 0, &abort_flag, &g_selftest_error, kErrTimeoutSelftest,
-                                  limit_ns);
-  if (ok && threadIdx.x == 0) atomicExch(&g_selftest_error, -1);  // must not happen
+  const ErrSink err{g_selftest_error, 1u};
+  const bool ok = mbar_wait_limit(bar, 0, &abort_flag, err, kErrTimeoutSelftest, limit_ns);
+  if (ok && threadIdx.x == 0) atomicExch(&g_selftest_error[0], -1);  // must not happen
 }
 
 }  // namespace

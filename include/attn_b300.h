@@ -17,8 +17,12 @@
  *   bit-identical outputs (except attn_bwd's dq at d = 128, see there).
  * - Errors: on invalid arguments nothing is launched and a non-zero status is
  *   returned; attn_last_error() then returns a human-readable message (per
- *   calling thread).  Kernels bound every internal wait; a wait that times
- *   out records a code read by attn_device_status().
+ *   calling thread).  Kernels bound every internal wait (2 s); a wait that
+ *   times out records a code that stays until attn_device_status() reads it,
+ *   and the outputs of that one launch are undefined.  Poll
+ *   attn_device_status() (it synchronises the stream) when a failed launch
+ *   must be detected; a status of ATTN_OK from a call only means the launch
+ *   was queued.  A timeout affects only the launch it happened in.
  *
  * Notation (source pages): Interview notes "他人面经整理", answer
  * "介绍你理解的flashattention", part 1 defines self-attention as
@@ -97,6 +101,17 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
  * Unknown flag bits give ATTN_EINVAL.  Everything else as attn_fwd.
  */
 #define ATTN_FWD_EXP2_FMA 1u
+/*
+ *   ATTN_FWD_DIAG_WAIT_EXPIRES  a failure-detection test, not for normal use
+ *       (the source pages have no counterpart).  In the first CTA, before any
+ *       copy or matrix product is issued, one bounded wait on a barrier that
+ *       nothing signals expires after 1 ms.  The launch then records a timeout
+ *       (code 0x105, read by attn_device_status) and its outputs are
+ *       undefined.  It shows that an expired wait is survived and stays
+ *       confined to its own launch: later calls, and calls on other streams,
+ *       compute normally without attn_device_status being called in between.
+ */
+#define ATTN_FWD_DIAG_WAIT_EXPIRES 2u
 ATTN_API attn_status attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                                  int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
                                  int causal, unsigned flags, attn_stream_t stream);
@@ -385,7 +400,9 @@ ATTN_API const char* attn_last_error(void);
  * attn_device_status -- synchronises `stream`, then reads and clears the
  * device error words the kernels set (a bounded wait that timed out, an
  * out-of-range block id).  Returns ATTN_OK, ATTN_EDEVICE (message holds the
- * code) or ATTN_ECUDA.  A debugging aid, not needed for normal operation.
+ * codes) or ATTN_ECUDA.  The words are shared by every stream and launch on
+ * the device and keep the first code recorded since the last read; the
+ * launch that recorded it has undefined outputs, other launches do not.
  */
 ATTN_API attn_status attn_device_status(attn_stream_t stream);
 

@@ -230,10 +230,11 @@ def test_selftest_rejects_bad_limit(lib):
 def test_attn_fwd_ex_flags(lib):
     a = dict(q=_fake(1), k=_fake(2), v=_fake(3), o=_fake(4))
     # unknown flag bits are rejected before anything else runs
-    st = lib.attn_fwd_ex(a["q"], a["k"], a["v"], a["o"], None, 1, 2, 2, 128, 128, 64,
-                         0.125, 0, 0x2, None)
-    assert st == binding.ATTN_EINVAL
-    assert b"flags" in lib.attn_last_error()
+    for bad in (0x4, 0x8, 0x80000000):
+        st = lib.attn_fwd_ex(a["q"], a["k"], a["v"], a["o"], None, 1, 2, 2, 128, 128, 64,
+                             0.125, 0, bad, None)
+        assert st == binding.ATTN_EINVAL
+        assert b"flags" in lib.attn_last_error()
 
 
 def _fwd_host(lib, **kw):

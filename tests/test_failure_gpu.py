@@ -3,8 +3,10 @@
 Every wait in the kernels is bounded.  attn_selftest_wait_timeout makes one
 such wait run out (a barrier that nothing signals, 20 ms limit) and checks
 that the expiry is recorded; afterwards the context must still run the
-normal kernels correctly.  Nothing here traps, asserts on the device or
-touches a bad address.
+normal kernels correctly.  ATTN_FWD_DIAG_WAIT_EXPIRES does the same inside a
+real prefill launch (1 ms limit), to check that the expiry only affects the
+launch it happened in.  Nothing here traps, asserts on the device or touches
+a bad address.
 """
 
 import math
@@ -33,3 +35,46 @@ def test_expired_wait_is_reported_and_the_context_survives():
     torch.cuda.synchronize()
     O, L = oracle.attention_ref(f64(q), f64(k), f64(v), 1 / math.sqrt(128), True)
     compare(f64(o.cpu()), f64(lse.cpu()), O, L, "after the self-test")
+
+
+def _case(seed):
+    q, k, v = workloads.prefill_inputs(1, 4, 2, 700, 700, 128, seed=seed)
+    O, L = oracle.attention_ref(f64(q), f64(k), f64(v), 1 / math.sqrt(128), True)
+    return (q.cuda(), k.cuda(), v.cuda()), (O, L)
+
+
+def test_a_timeout_stays_inside_its_launch():
+    """attn_fwd_ex(ATTN_FWD_DIAG_WAIT_EXPIRES) lets one bounded wait of a real
+    prefill launch expire (CTA 0, before any copy or product is issued).
+    The next launch, with no attn_device_status in between, must compute the
+    right result: the timeout skips work only in the launch that recorded
+    it.  attn_device_status then reports the code once."""
+    (q, k, v), (O, L) = _case(5)
+    assert binding.device_status() == binding.ATTN_OK
+    binding.attn_fwd(q, k, v, causal=True, diag_wait_expires=True)
+    o, lse = binding.attn_fwd(q, k, v, causal=True)
+    o2, lse2 = binding.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    compare(f64(o.cpu()), f64(lse.cpu()), O, L, "launch after a timed-out launch")
+    compare(f64(o2.cpu()), f64(lse2.cpu()), O, L, "second launch after a timed-out launch")
+    assert binding.device_status() == binding.ATTN_EDEVICE
+    assert "0x105" in binding.load_library().attn_last_error().decode()
+    assert binding.device_status() == binding.ATTN_OK
+
+
+def test_a_timeout_does_not_void_another_streams_launch():
+    """A launch whose wait expires on one stream, and a normal launch queued
+    right behind it on a second stream (they can run at the same time): the
+    second one computes the right result."""
+    (q, k, v), (O, L) = _case(6)
+    assert binding.device_status() == binding.ATTN_OK
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s1):
+        binding.attn_fwd(q, k, v, causal=True, diag_wait_expires=True, stream=s1)
+    with torch.cuda.stream(s2):
+        o, lse = binding.attn_fwd(q, k, v, causal=True, stream=s2)
+    torch.cuda.synchronize()
+    compare(f64(o.cpu()), f64(lse.cpu()), O, L, "other stream during a timed-out launch")
+    assert binding.device_status() == binding.ATTN_EDEVICE
+    assert binding.device_status() == binding.ATTN_OK
