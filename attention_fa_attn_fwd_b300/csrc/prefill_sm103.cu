@@ -213,7 +213,9 @@ __global__ void __launch_bounds__(384, 1)
   const int h = bh % a.H;
   const int g_kv = h / (a.H / a.Hkv);
   const int zkv = b * a.Hkv + g_kv;
-  const bool dead = err.this_launch_timed_out();
+  // Whether a wait of this launch already expired: loaded here, used after
+  // the set-up barrier, so the load's latency overlaps the set-up.
+  const unsigned timed_out_launch = reinterpret_cast<const volatile unsigned*>(err.word)[1];
   // Keys of this sequence; the paged variant reads its own length.
   int Nk = a.Nk;
   int nblk = 0;  // paged: cached blocks of this sequence
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(384, 1)
     const int r0 = q0 + i * 128;
     int kv_end = Nk;
     if (a.causal) kv_end = min(Nk, r0 + 128 + (Nk - a.Nq));
-    n_t[i] = (r0 < a.Nq && kv_end > 0 && !dead) ? (kv_end + 127) / 128 : 0;
+    n_t[i] = (r0 < a.Nq && kv_end > 0) ? (kv_end + 127) / 128 : 0;
   }
   int n_kv = max(n_t[0], n_t[1]);
 
@@ -246,11 +248,33 @@ __global__ void __launch_bounds__(384, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
-    prefetch_tmap(&tm_o);
+  // The first copies (Q tiles, and K_0 when K is contiguous) leave before the
+  // CTA-wide barrier below, from the thread that initialised the barriers, so
+  // their latency overlaps the TMEM allocation and the rest of the set-up
+  // (about 1.2 us per CTA, a large share of a short causal tile pair).
+  const bool early = n_kv > 0 && (a.diag_wait_ns == 0 || blockIdx.x != 0);
+  if (warp == 0) {
+    __syncwarp();
+    if (early) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (n_t[i] == 0) continue;
+        mbar_arrive_expect_tx_elect(bar(C::kBarQF + i), C::kTileBytes);
+        for (int s = 0; s < C::kSlabs; ++s)
+          tma_load_3d_elect(sbase + C::kOffQ + i * C::kTileBytes + s * C::kSlabBytes, &tm_q,
+                            bar(C::kBarQF + i), s * 64, q0 + i * 128, bh);
+      }
+      if constexpr (!kPaged) {
+        mbar_arrive_expect_tx_elect(bar(C::kBarKF), C::kTileBytes);
+        for (int s = 0; s < C::kSlabs; ++s)
+          tma_load_3d_elect(sbase + C::kOffK + s * C::kSlabBytes, &tm_k, bar(C::kBarKF), s * 64, 0,
+                            zkv);
+      }
+    }
+    if (lane == 0) {
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_o);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -260,6 +284,20 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // A wait of this launch already expired: skip the work (after the early
+  // copies have landed, so none is in flight when the CTA exits).
+  const bool dead = timed_out_launch == a.launch_id;
+  if (dead) {
+    if (warp == 0 && early) {
+      const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
+      for (int i = 0; i < 2; ++i)
+        if (n_t[i] > 0) mbar_wait_drain(bar(C::kBarQF + i), 0, deadline);
+      if (!kPaged) mbar_wait_drain(bar(C::kBarKF), 0, deadline);
+    }
+    n_t[0] = n_t[1] = 0;
+    n_kv = 0;
+  }
 
   // Failure-detection test (attn_fwd_ex with ATTN_FWD_DIAG_WAIT_EXPIRES): in
   // CTA 0, before any copy or MMA is issued, one thread waits on a barrier
@@ -287,7 +325,7 @@ __global__ void __launch_bounds__(384, 1)
         bool ok = true;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-          if (n_t[i] == 0) continue;
+          if (n_t[i] == 0 || early) continue;  // early: issued before the set-up barrier
           mbar_arrive_expect_tx_elect(bar(C::kBarQF + i), C::kTileBytes);
           for (int s = 0; s < C::kSlabs; ++s)
             tma_load_3d_elect(sbase + C::kOffQ + i * C::kTileBytes + s * C::kSlabBytes, &tm_q,
@@ -330,14 +368,16 @@ __global__ void __launch_bounds__(384, 1)
           // stage (issued back to back, so they land together): the MMA warp's
           // wait for V_j before P V also covers the Q K^T on K_{j+1} that
           // follows it, one wait per step fewer.
-          bool k0_issued = false;
+          bool k0_issued = early;  // K_0 left with the Q tiles
           int prow = prow_of(0);
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarKE), 1, abort_flag, err,
-                                                 kErrTimeoutProducer));
-          if (ok) {
-            mbar_arrive_expect_tx_elect(bar(C::kBarKF), C::kTileBytes);
-            load_tile(&tm_k, sbase + C::kOffK, bar(C::kBarKF), 0, prow);
-            k0_issued = true;
+          if (!k0_issued) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarKE), 1, abort_flag, err,
+                                                   kErrTimeoutProducer));
+            if (ok) {
+              mbar_arrive_expect_tx_elect(bar(C::kBarKF), C::kTileBytes);
+              load_tile(&tm_k, sbase + C::kOffK, bar(C::kBarKF), 0, prow);
+              k0_issued = true;
+            }
           }
           for (int j = 0; ok && j < n_kv; ++j) {
             const int vs = j % C::kVStages;
@@ -659,17 +699,20 @@ __global__ void __launch_bounds__(384, 1)
     uint8_t* stage = smem + C::kOffQ + wg * C::kTileBytes;  // Q_i is no longer read
     if (ok) {
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      // The whole O row in one round trip (all loads issued, one wait).
+      uint32_t orow[D];
+      if (n > 0) {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(lane_base + col_o + c0, orow + c0);
+        tmem_ld_wait();
+        reg_fence<D>(orow);
+      } else {
+#pragma unroll
+        for (int e = 0; e < D; ++e) orow[e] = 0u;
+      }
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        if (n > 0) {
-          tmem_ld32(lane_base + col_o + c0, o);
-          tmem_ld_wait();
-          reg_fence<32>(o);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
+        const uint32_t* o = orow + c0;
         uint32_t pw[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
