@@ -62,6 +62,10 @@ struct DArgs {
   int H, Hkv, G, num_blocks, max_blocks, bps, max_splits;
   float c_log2;
   unsigned launch_id;  // set per kernel launch (see ErrSink)
+  // One split per sequence (max_splits == 1): the split kernel writes the
+  // final output itself and no merge kernel runs.
+  uint16_t* out_o;     // [S, H, D] bf16, or nullptr (partials + merge)
+  float* out_lse;      // [S, H] or nullptr
 };
 
 __device__ __forceinline__ void mma_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
@@ -107,7 +111,15 @@ __global__ void __launch_bounds__(128)
   const int seq_len = a.seq_lens[s];
   const int nblk = min((max(seq_len, 0) + kBlockTokens - 1) / kBlockTokens, a.max_blocks);
   const int b_lo = r * a.bps;
-  if (b_lo >= nblk) return;  // split past the end of this sequence: no partial
+  if (b_lo >= nblk) {  // split past the end of this sequence: no partial
+    if (a.out_o != nullptr && r == 0) {  // single-split output of an empty sequence
+      for (int idx = threadIdx.x; idx < a.G * D; idx += blockDim.x)
+        a.out_o[(size_t(s) * a.H + size_t(g) * a.G + idx / D) * D + idx % D] = 0;
+      if (a.out_lse != nullptr && threadIdx.x < a.G)
+        a.out_lse[size_t(s) * a.H + size_t(g) * a.G + threadIdx.x] = -INFINITY;
+    }
+    return;
+  }
   if (err.this_launch_timed_out()) return;  // partial left unwritten; error already recorded
   const int b_hi = min(nblk, b_lo + a.bps);
 
@@ -315,6 +327,13 @@ __global__ void __launch_bounds__(128)
       L += wgt * red_ml[(w * 8 + hr) * 2 + 1];
     }
     const size_t head = size_t(s) * a.H + size_t(g) * a.G + hr;
+    if (a.out_o != nullptr) {  // the only split: final normalised output
+      const float inv = (L > 0.f) ? 1.f / L : 0.f;
+      a.out_o[head * D + dcol] = uint16_t(pack_bf16x2(acc * inv, 0.f) & 0xffffu);
+      if (dcol == 0 && a.out_lse != nullptr)
+        a.out_lse[head] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+      continue;
+    }
     a.ws_o[(head * a.max_splits + r) * D + dcol] = acc;
     if (dcol == 0) {
       a.ws_ml[(head * a.max_splits + r) * 2 + 0] = M;
@@ -425,11 +444,14 @@ cudaError_t launch(const void* q, const void* k_cache, const void* v_cache, cons
   a.bps = plan.blocks_per_split;
   a.max_splits = plan.max_splits;
   a.c_log2 = scale * kLog2e;
+  const bool direct = plan.max_splits == 1;
+  a.out_o = direct ? static_cast<uint16_t*>(o) : nullptr;
+  a.out_lse = direct ? lse : nullptr;
   dim3 grid(plan.max_splits, Hkv, S);
   a.launch_id = next_launch_id();
   decode_split_kernel<D><<<grid, 128, C::kSmemBytes, stream>>>(tk, tv, a);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || direct) return e;
   const int warps = S * H;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((warps + 7) / 8);
@@ -447,13 +469,18 @@ cudaError_t launch(const void* q, const void* k_cache, const void* v_cache, cons
 }  // namespace
 
 DecodePlan decode_plan(int num_seqs, int H, int Hkv, int d, int max_blocks_per_seq) {
-  // Blocks per split: 64 (1024 tokens) unless that leaves fewer than ~4 CTAs
-  // per SM for sequences of half the maximum length; never below 4.  (On
-  // the 64-sequence workload 64 blocks beat 32: 174 vs 182 us, fewer
-  // partials to write and merge; 128 was no faster.)
-  int bps = 64;
-  const long long target = 4LL * 148;
-  while (bps > 4) {
+  // Blocks per split: 128 (2048 tokens), halved while that would give fewer
+  // than two CTAs per SM for sequences of half the table's length; never
+  // below 8.  Long splits win wherever the grid still covers the machine:
+  // on 64 sequences x 8 KV heads, 128-block splits against 8-block ones took
+  // 34.8 vs 43.0 us at 512 tokens and 53.3 vs 73.7 us at 1024 (fewer CTAs
+  // to set up, fewer partials to write and merge), and equal times from
+  // 2048 tokens on.  Small batches keep enough CTAs through the halving.
+  // At most 128: each warp keeps the physical ids of its blocks one per lane
+  // (4 warps x 32 lanes).
+  int bps = kWarps * 32;
+  const long long target = 2LL * 148;
+  while (bps > 8) {
     const long long splits = (max_blocks_per_seq / 2 + bps - 1) / bps;
     if (splits * num_seqs * Hkv >= target) break;
     bps /= 2;

@@ -173,3 +173,36 @@ def test_full_block_table_and_exact_block_boundaries():
     O, L = _ref(pb2, 1 / math.sqrt(128))
     compare(f64(o), f64(lse), O, L, "full table / block boundaries")
     assert binding.device_status() == binding.ATTN_OK
+
+
+def _with_lens_and_width(pb, lens, width):
+    """The same pool and sequences with new lengths and a block table widened
+    to `width` columns (extra columns point at block 0 and are never read)."""
+    bt = torch.zeros(pb.num_seqs, width, dtype=torch.int32)
+    w = min(width, pb.block_table.shape[1])
+    bt[:, :w] = pb.block_table[:, :w]
+    return workloads.PagedBatch(q=pb.q, k_cache=pb.k_cache, v_cache=pb.v_cache, block_table=bt,
+                                seq_lens=lens, block_size=16, logical_ids=pb.logical_ids,
+                                perm=pb.perm, k_unique=pb.k_unique, v_unique=pb.v_unique,
+                                num_unique=pb.num_unique)
+
+
+def test_single_split_and_multi_split_paths():
+    """A batch whose table is at most 128 blocks wide gets one split per
+    sequence (the split kernel writes the output itself, no merge); the same
+    batch behind a 600-column table is split and merged.  Both match the
+    oracle, including empty and one-token sequences."""
+    pb = workloads.paged_decode_inputs(num_seqs=40, H=32, Hkv=8, d=128, min_len=1, max_len=2000,
+                                       group=4, shared_tokens=64, seed=12)
+    lens = pb.seq_lens.clone()
+    lens[0], lens[1], lens[7] = 0, min(int(lens[1]), 1), min(int(lens[7]), 17)
+    assert pb.block_table.shape[1] <= 128
+    for width in (pb.block_table.shape[1], 600):
+        pbw = _with_lens_and_width(pb, lens, width)
+        per_split = pbw.num_seqs * 32 * (128 + 2) * 4
+        splits = binding.paged_decode_workspace_size(pbw.num_seqs, 32, 8, 128, width) // per_split
+        assert (splits == 1) == (width <= 128), (width, splits)
+        o, lse = _gpu(pbw)
+        assert torch.all(o[0].float() == 0) and torch.all(torch.isneginf(lse[0]))
+        O, L = _ref(pbw, 1 / math.sqrt(128))
+        compare(f64(o[1:]), f64(lse[1:]), O[1:], L[1:], f"{splits} split(s) per sequence")
