@@ -347,114 +347,82 @@ __global__ void __launch_bounds__(384, 1)
         };
         const int32_t* bt = nullptr;
         if constexpr (kPaged) bt = a.block_table + size_t(b) * a.max_blocks;
-        if constexpr (!kPaged) {
-          // Paged: pool row of this lane's block of tile j (lanes 0..7).
-          auto prow_of = [&](int j) -> int {
-            int prow = 0;
-            if constexpr (kPaged) {
-              prow = a.oob_row;
-              const int lb = j * 8 + lane;
-              if (lane < 8 && lb < nblk) {
-                const int phys = bt[lb];
-                if (phys >= 0 && phys < a.num_blocks)
-                  prow = (phys * a.Hkv + g_kv) * kPageTokens;
-                else
-                  err.record(kErrPagedBadBlock);
-              }
-            }
-            return prow;
-          };
-          // K_0 on K-full 0; then V_j and K_{j+1} together on V-full of V_j's
-          // stage (issued back to back, so they land together): the MMA warp's
-          // wait for V_j before P V also covers the Q K^T on K_{j+1} that
-          // follows it, one wait per step fewer.
-          bool k0_issued = early;  // K_0 left with the Q tiles
-          int prow = prow_of(0);
-          if (!k0_issued) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarKE), 1, abort_flag, err,
-                                                   kErrTimeoutProducer));
-            if (ok) {
-              mbar_arrive_expect_tx_elect(bar(C::kBarKF), C::kTileBytes);
-              load_tile(&tm_k, sbase + C::kOffK, bar(C::kBarKF), 0, prow);
-              k0_issued = true;
+        // Paged: lanes 0..7 hold the physical ids of tile t's 8 blocks.  The
+        // ids of tile j+2 are loaded while tile j's copies are issued, so the
+        // table lookups stay off the path between a stage freeing and its
+        // next copy.
+        auto phys_of = [&](int t) -> int {
+          int phys = -1;
+          if constexpr (kPaged) {
+            const int lb = t * 8 + lane;
+            if (lane < 8 && t < n_kv && lb < nblk) phys = bt[lb];
+          }
+          return phys;
+        };
+        // Pool row of this lane's block (blocks past the sequence end, and
+        // bad ids, read the zero-filled row past the pool).
+        auto prow_from = [&](int t, int phys) -> int {
+          int prow = 0;
+          if constexpr (kPaged) {
+            prow = a.oob_row;
+            if (lane < 8 && t * 8 + lane < nblk) {
+              if (phys >= 0 && phys < a.num_blocks)
+                prow = (phys * a.Hkv + g_kv) * kPageTokens;
+              else
+                err.record(kErrPagedBadBlock);
             }
           }
-          for (int j = 0; ok && j < n_kv; ++j) {
-            const int vs = j % C::kVStages;
-            const bool next = j + 1 < n_kv;
-            const int ks1 = (j + 1) % C::kKStages;
-            const int prow_next = next ? prow_of(j + 1) : 0;
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(bar(C::kBarVE + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag,
-                                      err, kErrTimeoutProducer));
+          return prow;
+        };
+        // K_0 on K-full 0; then V_j and K_{j+1} together on V-full of V_j's
+        // stage (issued back to back, so they land together): the MMA warp's
+        // wait for V_j before P V also covers the Q K^T on K_{j+1} that
+        // follows it, one wait per step fewer.
+        bool k0_issued = early && !kPaged;  // contiguous K_0 left with the Q tiles
+        int phys_next = phys_of(1);
+        int prow = prow_from(0, phys_of(0));
+        if (!k0_issued) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarKE), 1, abort_flag, err,
+                                                 kErrTimeoutProducer));
+          if (ok) {
+            mbar_arrive_expect_tx_elect(bar(C::kBarKF), C::kTileBytes);
+            load_tile(&tm_k, sbase + C::kOffK, bar(C::kBarKF), 0, prow);
+            k0_issued = true;
+          }
+        }
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int vs = j % C::kVStages;
+          const bool next = j + 1 < n_kv;
+          const int ks1 = (j + 1) % C::kKStages;
+          const int phys_after = phys_of(j + 2);  // used one iteration later
+          const int prow_next = next ? prow_from(j + 1, phys_next) : 0;
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(bar(C::kBarVE + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag,
+                                    err, kErrTimeoutProducer));
+          if (!ok) break;
+          if (next) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarKE + ks1),
+                                                   (((j + 1) / C::kKStages) & 1) ^ 1, abort_flag,
+                                                   err, kErrTimeoutProducer));
             if (!ok) break;
-            if (next) {
-              ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarKE + ks1),
-                                                     (((j + 1) / C::kKStages) & 1) ^ 1, abort_flag,
-                                                     err, kErrTimeoutProducer));
-              if (!ok) break;
-            }
-            mbar_arrive_expect_tx_elect(bar(C::kBarVF + vs), (next ? 2 : 1) * C::kTileBytes);
-            load_tile(&tm_v, sbase + C::kOffV + vs * C::kTileBytes, bar(C::kBarVF + vs), j, prow);
-            if (next)
-              load_tile(&tm_k, sbase + C::kOffK + ks1 * C::kTileBytes, bar(C::kBarVF + vs), j + 1,
-                        prow_next);
-            v_issued = j + 1;
-            prow = prow_next;
           }
-          if (!ok) {
-            // Abort path: let every copy already in flight land before exit.
-            const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
-            for (int i = 0; i < 2; ++i)
-              if (n_t[i] > 0) mbar_wait_drain(bar(C::kBarQF + i), 0, deadline);
-            if (k0_issued) mbar_wait_drain(bar(C::kBarKF), 0, deadline);
-            for (int j = max(0, v_issued - C::kVStages); j < v_issued; ++j)
-              mbar_wait_drain(bar(C::kBarVF + j % C::kVStages), (j / C::kVStages) & 1, deadline);
-          }
-        } else {
-          // Paged: K_j and V_j on their own barriers; the block-table lookups
-          // of tile j sit right before its loads, and pairing V_j with K_{j+1}
-          // would put K_{j+1}'s lookups on V_j's path (measured slower).
-          int k_issued = 0;
-          for (int j = 0; j < n_kv; ++j) {
-            const int ks = j % C::kKStages, vs = j % C::kVStages;
-            int prow = 0;
-            if constexpr (kPaged) {
-              prow = a.oob_row;
-              const int lb = j * 8 + lane;
-              if (lane < 8 && lb < nblk) {
-                const int phys = bt[lb];
-                if (phys >= 0 && phys < a.num_blocks)
-                  prow = (phys * a.Hkv + g_kv) * kPageTokens;
-                else
-                  err.record(kErrPagedBadBlock);
-              }
-            }
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(bar(C::kBarKE + ks), ((j / C::kKStages) & 1) ^ 1, abort_flag,
-                                      err, kErrTimeoutProducer));
-            if (!ok) break;
-            mbar_arrive_expect_tx_elect(bar(C::kBarKF + ks), C::kTileBytes);
-            load_tile(&tm_k, sbase + C::kOffK + ks * C::kTileBytes, bar(C::kBarKF + ks), j, prow);
-            k_issued = j + 1;
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(bar(C::kBarVE + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag,
-                                      err, kErrTimeoutProducer));
-            if (!ok) break;
-            mbar_arrive_expect_tx_elect(bar(C::kBarVF + vs), C::kTileBytes);
-            load_tile(&tm_v, sbase + C::kOffV + vs * C::kTileBytes, bar(C::kBarVF + vs), j, prow);
-            v_issued = j + 1;
-          }
-          if (!ok) {
-            // Abort path: let every copy already in flight land before exit.
-            const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
-            for (int i = 0; i < 2; ++i)
-              if (n_t[i] > 0) mbar_wait_drain(bar(C::kBarQF + i), 0, deadline);
-            for (int j = max(0, k_issued - C::kKStages); j < k_issued; ++j)
-              mbar_wait_drain(bar(C::kBarKF + j % C::kKStages), (j / C::kKStages) & 1, deadline);
-            for (int j = max(0, v_issued - C::kVStages); j < v_issued; ++j)
-              mbar_wait_drain(bar(C::kBarVF + j % C::kVStages), (j / C::kVStages) & 1, deadline);
-          }
+          mbar_arrive_expect_tx_elect(bar(C::kBarVF + vs), (next ? 2 : 1) * C::kTileBytes);
+          load_tile(&tm_v, sbase + C::kOffV + vs * C::kTileBytes, bar(C::kBarVF + vs), j, prow);
+          if (next)
+            load_tile(&tm_k, sbase + C::kOffK + ks1 * C::kTileBytes, bar(C::kBarVF + vs), j + 1,
+                      prow_next);
+          v_issued = j + 1;
+          prow = prow_next;
+          phys_next = phys_after;
+        }
+        if (!ok) {
+          // Abort path: let every copy already in flight land before exit.
+          const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
+          for (int i = 0; i < 2; ++i)
+            if (n_t[i] > 0) mbar_wait_drain(bar(C::kBarQF + i), 0, deadline);
+          if (k0_issued) mbar_wait_drain(bar(C::kBarKF), 0, deadline);
+          for (int j = max(0, v_issued - C::kVStages); j < v_issued; ++j)
+            mbar_wait_drain(bar(C::kBarVF + j % C::kVStages), (j / C::kVStages) & 1, deadline);
         }
       }
     } else if (warp == 1) {
@@ -477,18 +445,11 @@ __global__ void __launch_bounds__(384, 1)
           if (j == 0 && !__all_sync(0xffffffffu, mbar_wait(bar(C::kBarQF + i), 0, abort_flag, err,
                                                            kErrTimeoutMma)))
             return false;
-          if constexpr (!kPaged) {
-            // K_j (j >= 1) landed with V_{j-1}, whose wait preceded this call.
-            if (j == 0 && !(i == 1 && n_t[0] > 0) &&
-                !__all_sync(0xffffffffu, mbar_wait(bar(C::kBarKF), 0, abort_flag, err,
-                                                   kErrTimeoutMma)))
-              return false;
-          } else {
-            if (!(i == 1 && j < n_t[0]) &&
-                !__all_sync(0xffffffffu, mbar_wait(bar(C::kBarKF + ks), (j / C::kKStages) & 1,
-                                                   abort_flag, err, kErrTimeoutMma)))
-              return false;
-          }
+          // K_j (j >= 1) landed with V_{j-1}, whose wait preceded this call.
+          if (j == 0 && !(i == 1 && n_t[0] > 0) &&
+              !__all_sync(0xffffffffu, mbar_wait(bar(C::kBarKF), 0, abort_flag, err,
+                                                 kErrTimeoutMma)))
+            return false;
           tc_fence_after();
           const uint32_t d_tmem = tmem + C::kColS + i * 128;
           const uint64_t qa = desc_add(q_desc, uint32_t((i * C::kTileBytes) >> 4));
