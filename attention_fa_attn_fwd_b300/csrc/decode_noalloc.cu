@@ -17,11 +17,17 @@
 //     results -- serialise them on one stream;
 //   * it keeps the previous call's contents; nothing in it needs to start at
 //     zero, because the merge kernel reads only partials that the split
-//     kernel of the same call has just written.
+//     kernel of the same call has just written -- when the call succeeds.
+//     After a call in which a bounded wait expired (attn_device_status then
+//     reports ATTN_EDEVICE), o and lse are undefined and may hold values
+//     computed from an earlier call's partials.
 // The host needs the array's device address, not the name: in host code the
 // name is a host-side stand-in.  The first call on each device therefore
 // looks the address up (cudaGetSymbolAddress, with that device current) and
-// caches it; make that first call before any stream capture.
+// caches it; make that first call before any stream capture.  The cached
+// address belongs to the device's current context: resetting the device
+// (cudaDeviceReset) after the first call is not supported, because later
+// calls would keep using the old address.
 
 #include <cstdio>
 #include <mutex>
@@ -78,6 +84,9 @@ attn_status paged_decode_noalloc(const void* q, const void* k_cache, const void*
   }
   if (need == 0) {
     // Invalid sizes: let paged_decode report exactly which argument is wrong.
+    // The stand-in workspace pointer below is never dereferenced: paged_decode
+    // rejects these sizes before it launches anything; it is non-null only so
+    // that the null-workspace check does not hide the real error.
     return paged_decode(q, k_cache, v_cache, block_table, seq_lens, num_seqs, H, Hkv, d,
                         num_blocks, max_blocks_per_seq, block_size, scale, o, lse,
                         reinterpret_cast<void*>(uintptr_t(256)), 0, stream);

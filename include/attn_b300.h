@@ -284,6 +284,11 @@ ATTN_API attn_status paged_decode(const void* q, const void* k_cache, const void
  *     results.  Serialise them on one stream.
  *   - The first call on each device looks the array's address up (once, with
  *     that device current); make that first call before any stream capture.
+ *     The address is kept for the rest of the process: do not reset the
+ *     device (cudaDeviceReset) after that first call.
+ *   - The array keeps the last call's contents.  After a call whose bounded
+ *     wait expired (attn_device_status reports ATTN_EDEVICE), o and lse are
+ *     undefined and may hold values from an earlier call.
  */
 ATTN_API attn_status paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                           const int32_t* block_table, const int32_t* seq_lens,

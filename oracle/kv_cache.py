@@ -19,9 +19,10 @@ here (the one the kernels implement):
   bookkeeping: a write into a block that other sequences still reference
   first copies the block into a fresh one (copy-on-write); a write into a
   block nobody else references happens in place; a write past the last block
-  takes a fresh block.  Fresh blocks come off the top of a free stack.  It
-  serves to pin the invariants the GPU's tables must satisfy; physical block
-  ids are an allocation detail and are not compared.
+  takes a fresh block.  Fresh blocks come off the top of a free stack, in
+  sequence order.  Because that order is fixed, the resulting tables --
+  physical block ids included --, reference counts and stack top are unique,
+  and the GPU tests compare all of them exactly with this manager's.
 """
 
 from __future__ import annotations
