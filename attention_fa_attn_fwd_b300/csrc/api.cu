@@ -354,7 +354,7 @@ attn_status paged_decode(const void* q, const void* k_cache, const void* v_cache
   if (!(scale > 0.f) || !(scale < 3.0e38f))
     return fail(ATTN_EINVAL, "paged_decode: scale must be positive and finite");
   if (d != 64 && d != 128) return fail(ATTN_EUNSUPPORTED, "paged_decode: head dim %d", d);
-  if (H / Hkv > 8) return fail(ATTN_EUNSUPPORTED, "paged_decode: H/Hkv=%d > 8", H / Hkv);
+  if (H / Hkv > 16) return fail(ATTN_EUNSUPPORTED, "paged_decode: H/Hkv=%d > 16", H / Hkv);
   if ((long long)num_blocks * Hkv * 16 >= (1LL << 31))
     return fail(ATTN_EINVAL, "paged_decode: KV pool too large for 32-bit row coordinates");
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||

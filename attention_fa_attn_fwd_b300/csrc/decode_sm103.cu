@@ -91,11 +91,15 @@ __device__ __forceinline__ uint32_t sw128(int row, int col) {
   return uint32_t(row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
 }
 
-template <int D>
+// kR16: G = H / Hkv > 8, so rows 8..15 of the 16-row mma tile are query heads
+// too (each lane then keeps the softmax state of rows gq and gq + 8); with
+// G <= 8 those rows are zero padding and their softmax is skipped.
+template <int D, bool kR16>
 __global__ void __launch_bounds__(128)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DArgs a) {
   using C = DCfg<D>;
+  constexpr int NR = kR16 ? 2 : 1;  // softmax rows per lane: gq (and gq + 8)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -142,22 +146,29 @@ __global__ void __launch_bounds__(128)
     const uint16_t* qrow = a.q + (size_t(s) * a.H + size_t(g) * a.G + gq) * D;
 #pragma unroll
     for (int kc = 0; kc < D / 16; ++kc) {
-      uint32_t lo = 0, hi = 0;
+      uint32_t lo = 0, hi = 0, lo8 = 0, hi8 = 0;
       if (gq < a.G) {
         lo = *reinterpret_cast<const uint32_t*>(qrow + kc * 16 + 2 * tq);
         hi = *reinterpret_cast<const uint32_t*>(qrow + kc * 16 + 8 + 2 * tq);
       }
+      if (kR16 && gq + 8 < a.G) {
+        lo8 = *reinterpret_cast<const uint32_t*>(qrow + 8 * D + kc * 16 + 2 * tq);
+        hi8 = *reinterpret_cast<const uint32_t*>(qrow + 8 * D + kc * 16 + 8 + 2 * tq);
+      }
       qa[kc][0] = lo;
-      qa[kc][1] = 0u;  // rows 8..15: padding (G <= 8)
+      qa[kc][1] = lo8;  // rows 8..15 (zero padding when G <= 8)
       qa[kc][2] = hi;
-      qa[kc][3] = 0u;
+      qa[kc][3] = hi8;
     }
   }
 
   float o[C::kDT][4];
 #pragma unroll
   for (int i = 0; i < C::kDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m = -INFINITY, l = 0.f;  // row gq; l is this lane's partial sum
+  // rows gq (and gq + 8); l is this lane's partial sum
+  float m[NR], l[NR];
+#pragma unroll
+  for (int rr = 0; rr < NR; ++rr) m[rr] = -INFINITY, l[rr] = 0.f;
 
   const int n_mine = (b_hi - b_lo - warp + kWarps - 1) / kWarps;  // blocks of this warp
   const uint32_t wbase = sbase + warp * C::kWarpBytes;
@@ -231,38 +242,40 @@ __global__ void __launch_bounds__(128)
         mma_16816(sc[1], qa[kc], bfr[2], bfr[3]);
       }
     }
-    // ---- online softmax on row gq (values c0, c1 of both token tiles)
-    float x[4];
+    // ---- online softmax on row gq (c0, c1 of both token tiles) and, with
+    // kR16, row gq + 8 (c2, c3)
+    uint32_t pa[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int rr = 0; rr < NR; ++rr) {
+      float x[4];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int tok = nt * 8 + 2 * tq + e;
-        x[nt * 2 + e] = (tok < valid) ? sc[nt][e] * a.c_log2 : -INFINITY;
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int tok = nt * 8 + 2 * tq + e;
+          x[nt * 2 + e] = (tok < valid) ? sc[nt][2 * rr + e] * a.c_log2 : -INFINITY;
+        }
+      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      if (mx > m[rr] + 8.0f) {  // move the reference (uniform across the row's 4 lanes)
+        const float alpha = ex2_approx(m[rr] - mx);
+        m[rr] = mx;
+        l[rr] *= alpha;
+#pragma unroll
+        for (int dt = 0; dt < C::kDT; ++dt) {
+          o[dt][2 * rr] *= alpha;
+          o[dt][2 * rr + 1] *= alpha;
+        }
       }
-    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    if (mx > m + 8.0f) {  // move the reference (uniform across the row's 4 lanes)
-      const float alpha = ex2_approx(m - mx);
-      m = mx;
-      l *= alpha;
+      const float nm = (m[rr] == -INFINITY) ? 0.f : -m[rr];
+      float p[4];
 #pragma unroll
-      for (int dt = 0; dt < C::kDT; ++dt) {
-        o[dt][0] *= alpha;
-        o[dt][1] *= alpha;
-      }
+      for (int e = 0; e < 4; ++e) p[e] = ex2_approx(x[e] + nm);
+      l[rr] += (p[0] + p[1]) + (p[2] + p[3]);
+      pa[rr] = pack_bf16x2(p[0], p[1]);      // row gq (+8), tokens 2tq, 2tq+1
+      pa[2 + rr] = pack_bf16x2(p[2], p[3]);  // row gq (+8), tokens 8+2tq, 9+2tq
     }
-    const float nm = (m == -INFINITY) ? 0.f : -m;
-    float p[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) p[e] = ex2_approx(x[e] + nm);
-    l += (p[0] + p[1]) + (p[2] + p[3]);
-    uint32_t pa[4];
-    pa[0] = pack_bf16x2(p[0], p[1]);  // row gq, tokens 2tq, 2tq+1
-    pa[1] = 0u;                       // rows 8..15: padding
-    pa[2] = pack_bf16x2(p[2], p[3]);  // row gq, tokens 8+2tq, 9+2tq
-    pa[3] = 0u;
     // ---- O += P V
     {
       const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
@@ -295,20 +308,24 @@ __global__ void __launch_bounds__(128)
 
   // ---- merge the 4 warps' states through shared memory (stage memory reuse)
   __syncthreads();
-  float* red_o = reinterpret_cast<float*>(smem);                 // [4 warps][8 rows][D]
-  float* red_ml = reinterpret_cast<float*>(smem + kWarps * 8 * D * 4);  // [4][8][2]
-  l += __shfl_xor_sync(0xffffffffu, l, 1);
-  l += __shfl_xor_sync(0xffffffffu, l, 2);
-  if (!ok) m = -INFINITY, l = 0.f;
-  if (gq < a.G) {
+  float* red_o = reinterpret_cast<float*>(smem);                   // [4 warps][16 rows][D]
+  float* red_ml = reinterpret_cast<float*>(smem + kWarps * 16 * D * 4);  // [4][16][2]
 #pragma unroll
-    for (int dt = 0; dt < C::kDT; ++dt) {
-      red_o[(warp * 8 + gq) * D + dt * 8 + 2 * tq] = o[dt][0];
-      red_o[(warp * 8 + gq) * D + dt * 8 + 2 * tq + 1] = o[dt][1];
-    }
-    if (tq == 0) {
-      red_ml[(warp * 8 + gq) * 2 + 0] = m;
-      red_ml[(warp * 8 + gq) * 2 + 1] = l;
+  for (int rr = 0; rr < NR; ++rr) {
+    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
+    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
+    if (!ok) m[rr] = -INFINITY, l[rr] = 0.f;
+    const int hr = gq + 8 * rr;
+    if (hr < a.G) {
+#pragma unroll
+      for (int dt = 0; dt < C::kDT; ++dt) {
+        red_o[(warp * 16 + hr) * D + dt * 8 + 2 * tq] = o[dt][2 * rr];
+        red_o[(warp * 16 + hr) * D + dt * 8 + 2 * tq + 1] = o[dt][2 * rr + 1];
+      }
+      if (tq == 0) {
+        red_ml[(warp * 16 + hr) * 2 + 0] = m[rr];
+        red_ml[(warp * 16 + hr) * 2 + 1] = l[rr];
+      }
     }
   }
   __syncthreads();
@@ -317,14 +334,14 @@ __global__ void __launch_bounds__(128)
     const int hr = idx / D, dcol = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_ml[(w * 8 + hr) * 2]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_ml[(w * 16 + hr) * 2]);
     float acc = 0.f, L = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      const float mw = red_ml[(w * 8 + hr) * 2];
+      const float mw = red_ml[(w * 16 + hr) * 2];
       const float wgt = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
-      acc += wgt * red_o[(w * 8 + hr) * D + dcol];
-      L += wgt * red_ml[(w * 8 + hr) * 2 + 1];
+      acc += wgt * red_o[(w * 16 + hr) * D + dcol];
+      L += wgt * red_ml[(w * 16 + hr) * 2 + 1];
     }
     const size_t head = size_t(s) * a.H + size_t(g) * a.G + hr;
     if (a.out_o != nullptr) {  // the only split: final normalised output
@@ -420,15 +437,16 @@ cudaError_t launch(const void* q, const void* k_cache, const void* v_cache, cons
   const uint32_t box[3] = {64, kBlockTokens, 1};
   if (!encode_tmap_bf16(&tk, k_cache, 3, dims, strides, box, true, err)) return cudaErrorInvalidValue;
   if (!encode_tmap_bf16(&tv, v_cache, 3, dims, strides, box, true, err)) return cudaErrorInvalidValue;
+  const bool r16 = H / Hkv > 8;
   static thread_local int configured_device[2] = {-1, -1};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (configured_device[D == 128] != dev) {
-    e = cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
+  if (configured_device[r16] != dev) {
+    e = cudaFuncSetAttribute(r16 ? decode_split_kernel<D, true> : decode_split_kernel<D, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured_device[D == 128] = dev;
+    configured_device[r16] = dev;
   }
   DArgs a;
   a.q = static_cast<const uint16_t*>(q);
@@ -449,7 +467,10 @@ cudaError_t launch(const void* q, const void* k_cache, const void* v_cache, cons
   a.out_lse = direct ? lse : nullptr;
   dim3 grid(plan.max_splits, Hkv, S);
   a.launch_id = next_launch_id();
-  decode_split_kernel<D><<<grid, 128, C::kSmemBytes, stream>>>(tk, tv, a);
+  if (r16)
+    decode_split_kernel<D, true><<<grid, 128, C::kSmemBytes, stream>>>(tk, tv, a);
+  else
+    decode_split_kernel<D, false><<<grid, 128, C::kSmemBytes, stream>>>(tk, tv, a);
   e = cudaGetLastError();
   if (e != cudaSuccess || direct) return e;
   const int warps = S * H;

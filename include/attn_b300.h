@@ -257,7 +257,7 @@ ATTN_API size_t paged_decode_workspace_size(int num_seqs, int H, int Hkv, int d,
  * read as zeros and recorded as a device error (attn_device_status).
  * A sequence of length 0 gets o = 0 and lse = -inf.
  *
- * Requirements: block_size == 16; H % Hkv == 0 and H / Hkv <= 8; d in
+ * Requirements: block_size == 16; H % Hkv == 0 and H / Hkv <= 16; d in
  * {64, 128}; num_blocks * Hkv * 16 < 2^31; pointers 16-byte aligned
  * (block_table, seq_lens and lse: 4-byte aligned).
  */

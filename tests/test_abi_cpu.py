@@ -92,7 +92,7 @@ def _dec(lib, **kw):
     (dict(S=0), binding.ATTN_EINVAL),
     (dict(bs=32), binding.ATTN_EINVAL),
     (dict(H=30), binding.ATTN_EINVAL),
-    (dict(H=64, Hkv=4), binding.ATTN_EUNSUPPORTED),
+    (dict(H=68, Hkv=4), binding.ATTN_EUNSUPPORTED),
     (dict(d=80), binding.ATTN_EUNSUPPORTED),
     (dict(wsb=16), binding.ATTN_EINVAL),
     (dict(scale=0.0), binding.ATTN_EINVAL),

@@ -39,7 +39,7 @@ SMALL = dict(num_seqs=8, H=8, Hkv=2, d=128, block_size=16, min_len=40, max_len=7
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("H,Hkv", [(8, 2), (8, 8), (8, 1), (6, 2)])
+@pytest.mark.parametrize("H,Hkv", [(8, 2), (8, 8), (8, 1), (6, 2), (16, 1), (24, 2), (12, 1), (32, 2)])
 def test_small_batch(d, H, Hkv):
     pb = workloads.paged_decode_inputs(**{**SMALL, "d": d, "H": H, "Hkv": Hkv}, seed=H + Hkv + d)
     o, lse = _gpu(pb)
@@ -55,10 +55,12 @@ def test_paged_decode_workload_full():
     compare(f64(o), f64(lse), O, L, "paged decode workload")
 
 
-def test_block_table_indexing_exact():
+@pytest.mark.parametrize("H,Hkv", [(32, 8), (32, 2)])
+def test_block_table_indexing_exact(H, Hkv):
     # One dominant key per sequence whose V row encodes its logical position:
-    # the bf16 output must equal that row exactly.
-    cfg = dict(workloads.PAGED_WORKLOADS["paged_decode_s64_h32kv8_d128"])
+    # the bf16 output must equal that row exactly (also with 16 query heads
+    # per KV head, where rows 8..15 of the mma tile are heads too).
+    cfg = dict(workloads.PAGED_WORKLOADS["paged_decode_s64_h32kv8_d128"], H=H, Hkv=Hkv)
     pb = workloads.paged_decode_inputs(**cfg, seed=5, index_probe=True)
     o, _ = _gpu(pb)
     of = f64(o)
