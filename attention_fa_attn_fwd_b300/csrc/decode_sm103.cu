@@ -128,48 +128,7 @@ __global__ void __launch_bounds__(128)
   const int b_hi = min(nblk, b_lo + a.bps);
 
   auto bar = [&](int w, int st) -> uint32_t { return sbase + C::kOffBar + 8u * (w * kRing + st); };
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kWarps * kRing; ++i) mbar_init(sbase + C::kOffBar + 8u * i, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (threadIdx.x == 32) {
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
-  }
-  __syncthreads();
-
   const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
-  // Q fragments (A operand, rows = heads of this group, zero beyond G).
-  uint32_t qa[D / 16][4];
-  {
-    const uint16_t* qrow = a.q + (size_t(s) * a.H + size_t(g) * a.G + gq) * D;
-#pragma unroll
-    for (int kc = 0; kc < D / 16; ++kc) {
-      uint32_t lo = 0, hi = 0, lo8 = 0, hi8 = 0;
-      if (gq < a.G) {
-        lo = *reinterpret_cast<const uint32_t*>(qrow + kc * 16 + 2 * tq);
-        hi = *reinterpret_cast<const uint32_t*>(qrow + kc * 16 + 8 + 2 * tq);
-      }
-      if (kR16 && gq + 8 < a.G) {
-        lo8 = *reinterpret_cast<const uint32_t*>(qrow + 8 * D + kc * 16 + 2 * tq);
-        hi8 = *reinterpret_cast<const uint32_t*>(qrow + 8 * D + kc * 16 + 8 + 2 * tq);
-      }
-      qa[kc][0] = lo;
-      qa[kc][1] = lo8;  // rows 8..15 (zero padding when G <= 8)
-      qa[kc][2] = hi;
-      qa[kc][3] = hi8;
-    }
-  }
-
-  float o[C::kDT][4];
-#pragma unroll
-  for (int i = 0; i < C::kDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  // rows gq (and gq + 8); l is this lane's partial sum
-  float m[NR], l[NR];
-#pragma unroll
-  for (int rr = 0; rr < NR; ++rr) m[rr] = -INFINITY, l[rr] = 0.f;
-
   const int n_mine = (b_hi - b_lo - warp + kWarps - 1) / kWarps;  // blocks of this warp
   const uint32_t wbase = sbase + warp * C::kWarpBytes;
   const int32_t* bt = a.block_table + size_t(s) * a.max_blocks;
@@ -196,11 +155,52 @@ __global__ void __launch_bounds__(128)
       tma_load_3d(dst + C::kKBytes + bx * C::kBoxBytes, &tm_v, bar(warp, st), bx * 64, row0, 0);
     }
   };
+  // Each warp's lane 0 initialises the warp's own ring barriers and issues
+  // its first copies straight away, before the CTA-wide barrier below (which
+  // only publishes the abort flag): the copies' latency overlaps the set-up
+  // and the Q loads.
+  if (lane == 0) {
+    for (int st = 0; st < kRing; ++st) mbar_init(bar(warp, st), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
 #pragma unroll
   for (int i = 0; i < kRing; ++i) {
     const int ph = __shfl_sync(0xffffffffu, my_phys, i);
     if (lane == 0 && i < n_mine) issue(i, ph);
   }
+
+  // Q fragments (A operand, rows = heads of this group, zero beyond G).
+  uint32_t qa[D / 16][4];
+  {
+    const uint16_t* qrow = a.q + (size_t(s) * a.H + size_t(g) * a.G + gq) * D;
+#pragma unroll
+    for (int kc = 0; kc < D / 16; ++kc) {
+      uint32_t lo = 0, hi = 0, lo8 = 0, hi8 = 0;
+      if (gq < a.G) {
+        lo = *reinterpret_cast<const uint32_t*>(qrow + kc * 16 + 2 * tq);
+        hi = *reinterpret_cast<const uint32_t*>(qrow + kc * 16 + 8 + 2 * tq);
+      }
+      if (kR16 && gq + 8 < a.G) {
+        lo8 = *reinterpret_cast<const uint32_t*>(qrow + 8 * D + kc * 16 + 2 * tq);
+        hi8 = *reinterpret_cast<const uint32_t*>(qrow + 8 * D + kc * 16 + 8 + 2 * tq);
+      }
+      qa[kc][0] = lo;
+      qa[kc][1] = lo8;  // rows 8..15 (zero padding when G <= 8)
+      qa[kc][2] = hi;
+      qa[kc][3] = hi8;
+    }
+  }
+  if (threadIdx.x == 0) *abort_flag = 0;
+  __syncthreads();
+
+  float o[C::kDT][4];
+#pragma unroll
+  for (int i = 0; i < C::kDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  // rows gq (and gq + 8); l is this lane's partial sum
+  float m[NR], l[NR];
+#pragma unroll
+  for (int rr = 0; rr < NR; ++rr) m[rr] = -INFINITY, l[rr] = 0.f;
 
   bool ok = true;
   int consumed = 0;
