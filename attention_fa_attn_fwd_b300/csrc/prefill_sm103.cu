@@ -164,6 +164,12 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // The first copies read the Q and K descriptors: fetch them while the
+  // rest of the set-up runs.
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+  }
 
   // Heavy (late, causal) tile pairs first; heads of one KV group adjacent.
   // group_major: all tile pairs of one (batch, KV head) group before the
@@ -239,14 +245,15 @@ __global__ void __launch_bounds__(384, 1)
   }
   int n_kv = max(n_t[0], n_t[1]);
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kNumBars; ++i) {
-      uint32_t count = 1;
-      if (i >= C::kBarPF && i < C::kBarPF2 + 2) count = 128;
-      mbar_init(bar(i), count);
-    }
-    *abort_flag = 0;
+  // Warp 0's lanes initialise one barrier each (one pass instead of a loop
+  // of ~30 in one thread).
+  static_assert(C::kNumBars <= 32, "one barrier per lane");
+  if (warp == 0) {
+    if (lane < C::kNumBars)
+      mbar_init(bar(lane), (lane >= C::kBarPF && lane < C::kBarPF2 + 2) ? 128u : 1u);
+    if (lane == 0) *abort_flag = 0;
     fence_mbar_init();
+    __syncwarp();
   }
   // The first copies (Q tiles, and K_0 when K is contiguous) leave before the
   // CTA-wide barrier below, from the thread that initialised the barriers, so
