@@ -791,7 +791,7 @@ __global__ void __launch_bounds__(384, 1)
 // between calls by fp32 rounding; dk and dv are accumulated in TMEM in a
 // fixed order and are bit-reproducible.
 //
-// Warps: 0 TMA producer, 1 MMA issuer, 2-3 idle, 4-7 compute half 0,
+// Warps: 0 TMA producer, 1-2 MMA issuers, 3 idle, 4-7 compute half 0,
 // 8-11 compute half 1, 12-15 dQ drain.
 struct FusedCfg : BCfg<128> {
   using B_ = BCfg<128>;
@@ -815,9 +815,11 @@ struct FusedCfg : BCfg<128> {
   static constexpr int kBarPF = kBarSF + 2;        // 2: P^T_h, dS^T_h written (128 arrivals)
   static constexpr int kBarDQF = kBarPF + 2;       // 2: dQ^T_h in TMEM
   static constexpr int kBarDQE = kBarDQF + 2;      // 2: dQ^T_h read out (128 arrivals)
-  static constexpr int kBarOF = kBarDQE + 2;       // dK, dV complete
-  static constexpr int kBarDrain = kBarOF + 1;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarSE = kBarDQE + 2;       // 2: dV, dK of half h done (S^T_h free)
+  static constexpr int kBarOF = kBarSE + 2;        // dK, dV complete
+  static constexpr int kBarDrain = kBarOF + 1;     // abort drains of the two MMA warps
+  static constexpr int kBarDrain2 = kBarDrain + 1;
+  static constexpr int kNumBars = kBarDrain2 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   // half h: S^T_h at h*128 (64 columns; P^T_h then dS^T_h as bf16 pairs over
@@ -904,6 +906,26 @@ __global__ void __launch_bounds__(512, 1)
       }
       bool ok = true;
       int issued = 0;
+      // The per-query statistics of half u are read from global memory one
+      // half ahead, so that their latency overlaps the wait for a free stage
+      // instead of delaying the copies.
+      float st_nl[2], st_dd[2];  // lse and D of this lane's two queries
+      auto load_stats = [&](int u) {
+        const int it = u >> 1;
+        const int hq = b * a.H + g * G + it / per_head;
+        const int r0 = (qt0 + it % per_head) * 128 + (u & 1) * 64;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int r = r0 + lane * 2 + e;
+          st_nl[e] = -INFINITY;
+          st_dd[e] = 0.f;
+          if (u < 2 * n_it && r < a.Nq) {
+            st_nl[e] = a.lse[size_t(hq) * a.Nq + r];
+            st_dd[e] = a.delta[size_t(hq) * a.Nq + r];
+          }
+        }
+      };
+      load_stats(0);
       for (int u = 0; u < 2 * n_it; ++u) {
         const int it = u >> 1, h = u & 1;
         const int hs = u % C::kHS;
@@ -916,14 +938,9 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int cidx = lane * 2 + e;
-          const int r = r0 + cidx;
-          float nl = -INFINITY, dd = 0.f;
-          if (r < a.Nq) {
-            nl = neg_lse2_of(a.lse[size_t(hq) * a.Nq + r]);
-            dd = a.delta[size_t(hq) * a.Nq + r];
-          }
-          sp[cidx] = nl;
-          sp[64 + cidx] = dd;
+          // lse = -inf past Nq (and on rows that see no key): P = 0 there
+          sp[cidx] = neg_lse2_of(st_nl[e]);
+          sp[64 + cidx] = st_dd[e];
         }
         if (lane == 0)
           mbar_arrive_expect_tx(bar(C::kBarQF + hs), 2 * C::kHalfBytes);
@@ -937,6 +954,7 @@ __global__ void __launch_bounds__(512, 1)
                             bar(C::kBarQF + hs), s * 64, r0, hq);
         }
         issued = u + 1;
+        load_stats(u + 1);
       }
       if (!ok) {
         const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
@@ -944,95 +962,103 @@ __global__ void __launch_bounds__(512, 1)
         for (int u = max(0, issued - C::kHS); u < issued; ++u)
           mbar_wait_drain(bar(C::kBarQF + u % C::kHS), (u / C::kHS) & 1, deadline);
       }
-    } else if (warp == 1 && n_it > 0) {
-      // ------------------------------------------------------ MMA issuer
-      constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, 0);
-      constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 1);
-      constexpr uint32_t kIdescDQ = idesc_bf16_f32_amn(128, 64, 1);
+    } else if ((warp == 1 || warp == 2) && n_it > 0) {
+      // ---------------------------------------------- MMA issuers (two warps)
+      // The tcgen05 queue holds only a few MMAs, and one warp that both
+      // issues and waits leaves the tensor pipe idle during every wait, even
+      // on a barrier whose phase completed long before (~250 cycles each,
+      // three per half, measured).  So two warps issue into the one pipe,
+      // each waiting while the other's products run:
+      //   warp 1: S^T(u), dP^T(u)           (waits: Q/dO loaded, S^T_h free,
+      //                                      dQ^T(u-2) read out)
+      //   warp 2: dV, dK (u), then dQ^T(u)  (wait: P^T, dS^T of u written)
+      // What a single issuing warp got from its issue order now comes from
+      // barriers: S^T(u) overwrites the P^T / dS^T of u - 2 only after
+      // dV, dK(u - 2) (kBarSE); dP^T(u) overwrites dQ^T(u - 2) only after the
+      // drain has read it (kBarDQE), which also means dQ^T(u - 2) is complete
+      // before the compute warpgroup of u writes dS^T_h again (it waits for
+      // dP^T(u)).  dV and dK are issued by warp 2 alone, in a fixed order.
       const uint64_t k_desc = smem_desc_sw128(sbase + C::kOffK, 16, 1024);
-      const uint64_t v_desc = smem_desc_sw128(sbase + C::kOffV, 16, 1024);
-      const uint64_t q_desc = smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
-      const uint64_t do_desc = smem_desc_sw128(sbase + C::kOffDO, 16, 1024);
-      const uint64_t qmn_desc = smem_desc_sw128(sbase + C::kOffQ, C::kHalfSlabBytes, 1024);
-      const uint64_t domn_desc = smem_desc_sw128(sbase + C::kOffDO, C::kHalfSlabBytes, 1024);
-      // K^T as an MN-major A operand (M = d: 64-column slabs kSlabBytes
-      // apart); dS^T as an MN-major B operand (N = 64 queries, one atom).
-      const uint64_t kmn_desc = smem_desc_sw128(sbase + C::kOffK, C::kSlabBytes, 1024);
-      const uint64_t ds_desc = smem_desc_sw128(sbase + C::kOffDS, C::kDSBytes, 1024);
-      // S^T_h = K Q[u]^T over the 64 queries of half u: two chains of four
-      // K-steps (32 bytes apart inside a 64-column slab; the second chain in
-      // the next slab).  Operand offsets are added inside the asm so the
-      // descriptors stay in a few registers.
-      auto issue_s = [&](int u) -> bool {
-        const int h = u & 1, hs = u % C::kHS;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarQF + hs), (u / C::kHS) & 1, abort_flag,
-                                               err, kErrTimeoutMma)))
+      auto wait_on = [&](int which, uint32_t parity) -> bool {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(bar(which), parity, abort_flag, err, kErrTimeoutMma)))
           return false;
         tc_fence_after();
-        const uint64_t qd = q_desc + uint64_t((hs * C::kHalfBytes) >> 4);
-        mma4_bf16_ss<2, 2>(tmem + h * 128, k_desc, qd, kIdescHalf, 0u);
-        mma4_bf16_ss<2, 2>(tmem + h * 128, k_desc + (C::kSlabBytes >> 4),
-                           qd + (C::kHalfSlabBytes >> 4), kIdescHalf, 1u);
         return true;
       };
-      // dP^T_h = V dO[u]^T into the half's second 64 columns, which hold
-      // dQ^T of half u - 2 until the drain warpgroup has read it.
-      auto issue_dp = [&](int u) -> bool {
-        const int h = u & 1, hs = u % C::kHS;
-        if (u >= 2) {
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarDQE + h), ((u >> 1) - 1) & 1,
-                                                 abort_flag, err, kErrTimeoutMma)))
-            return false;
-          tc_fence_after();
+      const int n_u = 2 * n_it;
+      bool ok = wait_on(C::kBarKVF, 0);
+      if (warp == 1) {
+        constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, 0);
+        const uint64_t v_desc = smem_desc_sw128(sbase + C::kOffV, 16, 1024);
+        const uint64_t q_desc = smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
+        const uint64_t do_desc = smem_desc_sw128(sbase + C::kOffDO, 16, 1024);
+        for (int u = 0; ok && u < n_u; ++u) {
+          const int h = u & 1, hs = u % C::kHS;
+          ok = wait_on(C::kBarQF + hs, (u / C::kHS) & 1);  // Q, dO of half u loaded
+          if (ok && u >= 2) ok = wait_on(C::kBarSE + h, ((u >> 1) - 1) & 1);  // dV, dK(u-2) done
+          if (!ok) break;
+          // S^T_h = K Q[u]^T over the 64 queries of half u: two chains of
+          // four K-steps (32 bytes apart inside a 64-column slab; the second
+          // chain in the next slab).
+          const uint64_t qd = q_desc + uint64_t((hs * C::kHalfBytes) >> 4);
+          mma4_bf16_ss<2, 2>(tmem + h * 128, k_desc, qd, kIdescHalf, 0u);
+          mma4_bf16_ss<2, 2>(tmem + h * 128, k_desc + (C::kSlabBytes >> 4),
+                             qd + (C::kHalfSlabBytes >> 4), kIdescHalf, 1u);
+          // dP^T_h = V dO[u]^T into the half's second 64 columns, which hold
+          // dQ^T of half u - 2 until the drain warpgroup has read it.
+          if (u >= 2) ok = wait_on(C::kBarDQE + h, ((u >> 1) - 1) & 1);
+          if (!ok) break;
+          const uint64_t dd = do_desc + uint64_t((hs * C::kHalfBytes) >> 4);
+          mma4_bf16_ss<2, 2>(tmem + h * 128 + 64, v_desc, dd, kIdescHalf, 0u);
+          mma4_bf16_ss<2, 2>(tmem + h * 128 + 64, v_desc + (C::kSlabBytes >> 4),
+                             dd + (C::kHalfSlabBytes >> 4), kIdescHalf, 1u);
+          mma_commit(bar(C::kBarSF + h));
         }
-        const uint64_t dd = do_desc + uint64_t((hs * C::kHalfBytes) >> 4);
-        mma4_bf16_ss<2, 2>(tmem + h * 128 + 64, v_desc, dd, kIdescHalf, 0u);
-        mma4_bf16_ss<2, 2>(tmem + h * 128 + 64, v_desc + (C::kSlabBytes >> 4),
-                           dd + (C::kHalfSlabBytes >> 4), kIdescHalf, 1u);
-        mma_commit(bar(C::kBarSF + h));
-        return true;
-      };
-      // dV += P^T_h dO[u], dK += dS^T_h Q[u] (frees the half-stage), then
-      // dQ^T_h = K^T dS^T_h (16 keys = 2048 bytes per MMA in both operands).
-      auto issue_acc = [&](int u) -> bool {
-        const int h = u & 1, hs = u % C::kHS;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF + h), (u >> 1) & 1, abort_flag, err,
-                                               kErrTimeoutMma)))
-          return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t o16 = uint32_t((hs * C::kHalfBytes + kk * 16 * 128) >> 4);
-          const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
-          mma_bf16_ts(tmem + C::kColDV, tmem + h * 128 + kk * 8, desc_add(domn_desc, o16), kIdescAcc,
-                      acc);
-          mma_bf16_ts(tmem + C::kColDK, tmem + h * 128 + 32 + kk * 8, desc_add(qmn_desc, o16),
-                      kIdescAcc, acc);
+        if (!ok) {
+          mma_commit(bar(C::kBarDrain));
+          mbar_wait_drain(bar(C::kBarDrain), 0, globaltimer_ns() + kWaitTimeoutNs);
         }
-        mma_commit(bar(C::kBarQE + hs));
-        const uint64_t dsd = ds_desc + uint64_t((h * C::kDSBytes) >> 4);
-        mma4_bf16_ss<128, 128>(tmem + h * 128 + 64, kmn_desc, dsd, kIdescDQ, 0u);
-        mma4_bf16_ss<128, 128>(tmem + h * 128 + 64, kmn_desc + 512, dsd + 512, kIdescDQ, 1u);
-        mma_commit(bar(C::kBarDQF + h));
-        return true;
-      };
-      bool ok = __all_sync(0xffffffffu,
-                           mbar_wait(bar(C::kBarKVF), 0, abort_flag, err, kErrTimeoutMma));
-      // Per (query head, query tile) it: S(u0) dP(u0) [acc(u0 - 1)] S(u1) dP(u1) acc(u0).
-      for (int it = 0; ok && it < n_it; ++it) {
-        ok = issue_s(2 * it);
-        if (ok) ok = issue_dp(2 * it);
-        if (ok && it > 0) ok = issue_acc(2 * it - 1);
-        if (ok) ok = issue_s(2 * it + 1);
-        if (ok) ok = issue_dp(2 * it + 1);
-        if (ok) ok = issue_acc(2 * it);
-      }
-      if (ok && n_it > 0) ok = issue_acc(2 * n_it - 1);
-      if (ok) {
-        mma_commit(bar(C::kBarOF));
       } else {
-        mma_commit(bar(C::kBarDrain));
-        mbar_wait_drain(bar(C::kBarDrain), 0, globaltimer_ns() + kWaitTimeoutNs);
+        constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 1);
+        constexpr uint32_t kIdescDQ = idesc_bf16_f32_amn(128, 64, 1);
+        const uint64_t qmn_desc = smem_desc_sw128(sbase + C::kOffQ, C::kHalfSlabBytes, 1024);
+        const uint64_t domn_desc = smem_desc_sw128(sbase + C::kOffDO, C::kHalfSlabBytes, 1024);
+        // K^T as an MN-major A operand (M = d: 64-column slabs kSlabBytes
+        // apart); dS^T as an MN-major B operand (N = 64 queries, one atom).
+        const uint64_t kmn_desc = smem_desc_sw128(sbase + C::kOffK, C::kSlabBytes, 1024);
+        const uint64_t ds_desc = smem_desc_sw128(sbase + C::kOffDS, C::kDSBytes, 1024);
+        for (int u = 0; ok && u < n_u; ++u) {
+          const int h = u & 1, hs = u % C::kHS;
+          ok = wait_on(C::kBarPF + h, (u >> 1) & 1);  // P^T, dS^T of half u written
+          if (!ok) break;
+          // dV += P^T_h dO[u], dK += dS^T_h Q[u]; then the half-stage and
+          // the S^T_h columns are free.  Queries 32c..32c+31 of the half
+          // have P^T in columns 32c..32c+15 of S^T_h and dS^T in the next 16
+          // (8 columns = 16 queries per K-step).
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t o16 = uint32_t((hs * C::kHalfBytes + kk * 16 * 128) >> 4);
+            const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t pcol = h * 128 + (kk >> 1) * 32 + (kk & 1) * 8;
+            mma_bf16_ts(tmem + C::kColDV, tmem + pcol, desc_add(domn_desc, o16), kIdescAcc, acc);
+            mma_bf16_ts(tmem + C::kColDK, tmem + pcol + 16, desc_add(qmn_desc, o16), kIdescAcc,
+                        acc);
+          }
+          mma_commit(bar(C::kBarQE + hs));
+          mma_commit(bar(C::kBarSE + h));
+          // dQ^T_h = K^T dS^T_h (16 keys = 2048 bytes per MMA in both operands).
+          const uint64_t dsd = ds_desc + uint64_t((h * C::kDSBytes) >> 4);
+          mma4_bf16_ss<128, 128>(tmem + h * 128 + 64, kmn_desc, dsd, kIdescDQ, 0u);
+          mma4_bf16_ss<128, 128>(tmem + h * 128 + 64, kmn_desc + 512, dsd + 512, kIdescDQ, 1u);
+          mma_commit(bar(C::kBarDQF + h));
+        }
+        if (ok) {
+          mma_commit(bar(C::kBarOF));
+        } else {
+          mma_commit(bar(C::kBarDrain2));
+          mbar_wait_drain(bar(C::kBarDrain2), 0, globaltimer_ns() + kWaitTimeoutNs);
+        }
       }
     }
   } else if (warp >= 12) {
@@ -1084,48 +1110,58 @@ __global__ void __launch_bounds__(512, 1)
                       mbar_wait(bar(C::kBarSF + wg), it & 1, abort_flag, err, kErrTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[64], p[64];
-      tmem_ld32(lane_base + wg * 128, s);
-      tmem_ld32(lane_base + wg * 128 + 32, s + 32);
-      tmem_ld32(lane_base + wg * 128 + 64, p);
-      tmem_ld32(lane_base + wg * 128 + 96, p + 32);
-      tmem_ld_wait();
-      reg_fence<64>(s);
-      reg_fence<64>(p);
       const float* nl = stat + hs * 128;
       const float* dd = nl + 64;
       const int lo = a.causal ? (kj - off - r0 - wg * 64) : -1;
       const bool key_ok = kj < a.Nk;
       const bool masked = !key_ok || lo > 0;
       const float2 c2 = make_float2(c, c);
-      const float2* nl2 = reinterpret_cast<const float2*>(nl);
-      const float2* dd2 = reinterpret_cast<const float2*>(dd);
-      uint32_t pp[32], pd[32];
+      // Two chunks of 32 queries, each finished (P^T and dS^T to TMEM, dS^T
+      // to shared memory) before the next is loaded: a third of the live
+      // registers of one pass over 64, so the exponentials of several
+      // columns overlap.
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])),
-                              c2, nl2[e]);
-        x.x = ex2_approx(x.x);
-        x.y = ex2_approx(x.y);
-        if (masked) {
-          if (!key_ok || 2 * e < lo) x.x = 0.f;
-          if (!key_ok || 2 * e + 1 < lo) x.y = 0.f;
+      for (int chk = 0; chk < 2; ++chk) {
+        uint32_t s[32], p[32];
+        tmem_ld32(lane_base + wg * 128 + chk * 32, s);
+        tmem_ld32(lane_base + wg * 128 + 64 + chk * 32, p);
+        tmem_ld_wait();
+        reg_fence<32>(s);
+        reg_fence<32>(p);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int el = 0; el < 16; ++el) {
+          const int e = chk * 16 + el;  // pair within the half
+          const float2 nlp = reinterpret_cast<const float2*>(nl)[e];
+          const float2 ddp = reinterpret_cast<const float2*>(dd)[e];
+          float2 x = __ffma2_rn(
+              make_float2(__uint_as_float(s[2 * el]), __uint_as_float(s[2 * el + 1])), c2, nlp);
+          x.x = ex2_approx(x.x);
+          x.y = ex2_approx(x.y);
+          if (masked) {
+            if (!key_ok || 2 * e < lo) x.x = 0.f;
+            if (!key_ok || 2 * e + 1 < lo) x.y = 0.f;
+          }
+          pp[el] = pack_bf16x2(x.x, x.y);
+          const float2 dp =
+              __fadd2_rn(make_float2(__uint_as_float(p[2 * el]), __uint_as_float(p[2 * el + 1])),
+                         make_float2(-ddp.x, -ddp.y));
+          const float2 d = __fmul2_rn(x, dp);
+          pd[el] = pack_bf16x2(d.x, d.y);
         }
-        pp[e] = pack_bf16x2(x.x, x.y);
-        const float2 ndd = dd2[e];
-        const float2 dp = __fadd2_rn(make_float2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])),
-                                     make_float2(-ndd.x, -ndd.y));
-        const float2 d = __fmul2_rn(x, dp);
-        pd[e] = pack_bf16x2(d.x, d.y);
-      }
-      // dS^T row (this key, 64 queries = 128 bytes) into the half's shared
-      // tile, 128-byte swizzled: the B operand of dQ^T.
+        // dS^T of these 32 queries (64 bytes of this key's row) into the
+        // half's shared tile, 128-byte swizzled: the B operand of dQ^T.
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(ds_row + ((ch ^ (row & 7)) << 4)) =
-            make_uint4(pd[4 * ch], pd[4 * ch + 1], pd[4 * ch + 2], pd[4 * ch + 3]);
-      tmem_st32(lane_base + wg * 128, pp);
-      tmem_st32(lane_base + wg * 128 + 32, pd);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int ch = chk * 4 + q4;
+          *reinterpret_cast<uint4*>(ds_row + ((ch ^ (row & 7)) << 4)) =
+              make_uint4(pd[4 * q4], pd[4 * q4 + 1], pd[4 * q4 + 2], pd[4 * q4 + 3]);
+        }
+        // P^T and dS^T of these 32 queries over the 32 S^T columns this
+        // chunk has just read (the other chunk's S^T stays intact).
+        tmem_st16(lane_base + wg * 128 + chk * 32, pp);
+        tmem_st16(lane_base + wg * 128 + chk * 32 + 16, pd);
+      }
       fence_proxy_async_smem();
       tmem_st_wait();
       tc_fence_before();
