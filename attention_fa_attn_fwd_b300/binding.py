@@ -28,6 +28,7 @@ ATTN_EDEVICE = 4
 ATTN_FWD_EXP2_FMA = 1  # attn_fwd_ex flags
 ATTN_FWD_DIAG_WAIT_EXPIRES = 2
 ATTN_BWD_DETERMINISTIC = 1  # attn_bwd_ex flag
+ATTN_BWD_DIAG_WAIT_EXPIRES = 2  # attn_bwd_ex flag: failure-detection test only
 _STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_EINVAL", 2: "ATTN_EUNSUPPORTED",
                  3: "ATTN_ECUDA", 4: "ATTN_EDEVICE"}
 
@@ -244,13 +245,15 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              scale: Optional[float] = None, dq: Optional[torch.Tensor] = None,
              dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
              workspace: Optional[torch.Tensor] = None, stream=None,
-             deterministic: bool = False):
+             deterministic: bool = False, diag_wait_expires: bool = False):
     """Gradients (dq, dk, dv) of ``attn_fwd`` via ``attn_bwd_ex``.
 
     q, o, do [B,H,Nq,d] bf16; k, v [B,Hkv,Nk,d] bf16; lse [B,H,Nq] fp32 from
     ``attn_fwd``.  ``workspace``: uint8 CUDA tensor of at least
     ``attn_bwd_workspace_size`` bytes (allocated here if omitted).
     ``deterministic`` sets ATTN_BWD_DETERMINISTIC (bit-reproducible dq).
+    ``diag_wait_expires`` adds ATTN_BWD_DIAG_WAIT_EXPIRES (a failure test:
+    one bounded wait of the call expires; its outputs are undefined).
     """
     lib = load_library()
     for t, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
@@ -275,7 +278,8 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     elif workspace.dtype != torch.uint8 or not workspace.is_cuda:
         raise TypeError("workspace must be a uint8 CUDA tensor")
-    flags = ATTN_BWD_DETERMINISTIC if deterministic else 0
+    flags = (ATTN_BWD_DETERMINISTIC if deterministic else 0) | \
+        (ATTN_BWD_DIAG_WAIT_EXPIRES if diag_wait_expires else 0)
     st = lib.attn_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                          B, H, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),

@@ -261,7 +261,7 @@ attn_status attn_bwd_ex(const void* q, const void* k, const void* v, const void*
   if (!(scale > 0.f) || !(scale < 3.0e38f))
     return fail(ATTN_EINVAL, "attn_bwd: scale must be positive and finite");
   if (causal != 0 && causal != 1) return fail(ATTN_EINVAL, "attn_bwd: causal must be 0 or 1");
-  if (flags & ~unsigned(ATTN_BWD_DETERMINISTIC))
+  if (flags & ~unsigned(ATTN_BWD_DETERMINISTIC | ATTN_BWD_DIAG_WAIT_EXPIRES))
     return fail(ATTN_EINVAL, "attn_bwd: unknown flags 0x%x", flags);
   if (d != 64 && d != 128) return fail(ATTN_EUNSUPPORTED, "attn_bwd: head dim %d (need 64 or 128)", d);
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
@@ -278,8 +278,10 @@ attn_status attn_bwd_ex(const void* q, const void* k, const void* v, const void*
   attn_status st = check_device();
   if (st != ATTN_OK) return st;
   const char* err = nullptr;
+  // The diagnostic wait's limit: 1 ms.
+  const unsigned diag_ns = (flags & ATTN_BWD_DIAG_WAIT_EXPIRES) ? 1000000u : 0u;
   cudaError_t e = attn::backward_launch(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, Nq, Nk, d,
-                                        scale, causal, det, workspace,
+                                        scale, causal, det, diag_ns, workspace,
                                         reinterpret_cast<cudaStream_t>(stream), &err);
   if (err) return fail(ATTN_ECUDA, "attn_bwd: %s", err);
   if (e != cudaSuccess) return fail(ATTN_ECUDA, "attn_bwd launch: %s", cudaGetErrorString(e));

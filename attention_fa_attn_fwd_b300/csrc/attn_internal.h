@@ -52,8 +52,8 @@ size_t backward_workspace_bytes(int B, int H, int Nq, int d, bool deterministic)
 cudaError_t backward_launch(const void* q, const void* k, const void* v, const void* o,
                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
                             int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
-                            bool deterministic, void* workspace, cudaStream_t stream,
-                            const char** err);
+                            bool deterministic, unsigned diag_wait_ns, void* workspace,
+                            cudaStream_t stream, const char** err);
 int backward_take_device_error();
 
 // ---- paged-cache append (kv_append.cu)

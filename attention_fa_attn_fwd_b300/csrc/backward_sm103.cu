@@ -103,7 +103,8 @@ struct BArgs {
   float c_log2;  // scale * log2(e)
   float scale;
   int causal;
-  unsigned launch_id;  // set per kernel launch (see ErrSink)
+  unsigned launch_id;     // set per kernel launch (see ErrSink)
+  unsigned diag_wait_ns;  // != 0: CTA 0 of the key-stationary kernel lets one wait expire
 };
 
 // -log2-domain LSE: P = 2^(s * c_log2 + neg_lse2).  A row with no key
@@ -470,7 +471,8 @@ struct DkvCfg : BCfg<D> {
   static constexpr int kBarPF = kBarSF + 2;         // 2: P^T_h, dS^T_h written (128 each)
   static constexpr int kBarOF = kBarPF + 2;         // dK, dV complete
   static constexpr int kBarDrain = kBarOF + 1;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarDiag = kBarDrain + 1;    // never signalled (diagnostic wait)
+  static constexpr int kNumBars = kBarDiag + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   // half h: S^T_h at h*128 (64 columns), dP^T_h at h*128 + 64; dV, dK after.
@@ -635,6 +637,14 @@ __global__ void __launch_bounds__(384, 1)
       // dV += P^T_h dO[h], dK += dS^T_h Q[h] (16 queries per MMA); frees the half-stage.
       auto issue_acc = [&](int u) -> bool {
         const int h = u & 1, hs = u % C::kHS;
+        // Failure-detection test (ATTN_BWD_DIAG_WAIT_EXPIRES): in CTA 0, a
+        // few halves in, a wait on a barrier nothing signals expires, with
+        // copies and products still in flight; every warp then drains.
+        if (a.diag_wait_ns != 0 && blockIdx.x == 0 && u == min(3, 2 * n_it - 1)) {
+          __all_sync(0xffffffffu, mbar_wait_limit(bar(C::kBarDiag), 0, abort_flag, err,
+                                                  kErrTimeoutDiag, a.diag_wait_ns));
+          return false;
+        }
         if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF + h), (u >> 1) & 1, abort_flag, err,
                                                kErrTimeoutMma)))
           return false;
@@ -819,7 +829,8 @@ struct FusedCfg : BCfg<128> {
   static constexpr int kBarOF = kBarSE + 2;        // dK, dV complete
   static constexpr int kBarDrain = kBarOF + 1;     // abort drains of the two MMA warps
   static constexpr int kBarDrain2 = kBarDrain + 1;
-  static constexpr int kNumBars = kBarDrain2 + 1;
+  static constexpr int kBarDiag = kBarDrain2 + 1;  // never signalled (diagnostic wait)
+  static constexpr int kNumBars = kBarDiag + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   // half h: S^T_h at h*128 (64 columns; P^T_h then dS^T_h as bf16 pairs over
@@ -1030,6 +1041,15 @@ __global__ void __launch_bounds__(512, 1)
         const uint64_t ds_desc = smem_desc_sw128(sbase + C::kOffDS, C::kDSBytes, 1024);
         for (int u = 0; ok && u < n_u; ++u) {
           const int h = u & 1, hs = u % C::kHS;
+          // Failure-detection test (ATTN_BWD_DIAG_WAIT_EXPIRES): in CTA 0, a
+          // few halves in, a wait on a barrier nothing signals expires, with
+          // copies and products still in flight; every warp then drains.
+          if (a.diag_wait_ns != 0 && blockIdx.x == 0 && u == min(3, n_u - 1)) {
+            __all_sync(0xffffffffu, mbar_wait_limit(bar(C::kBarDiag), 0, abort_flag, err,
+                                                    kErrTimeoutDiag, a.diag_wait_ns));
+            ok = false;
+            break;
+          }
           ok = wait_on(C::kBarPF + h, (u >> 1) & 1);  // P^T, dS^T of half u written
           if (!ok) break;
           // dV += P^T_h dO[u], dK += dS^T_h Q[u]; then the half-stage and
@@ -1247,7 +1267,8 @@ template <int D>
 cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o,
                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
                        int H, int Hkv, int Nq, int Nk, float scale, int causal, float* delta,
-                       float* dq_acc, cudaStream_t stream, const char** err) {
+                       float* dq_acc, unsigned diag_wait_ns, cudaStream_t stream,
+                       const char** err) {
   const uint32_t box[3] = {64, 128, 1};
   const uint64_t dq_[3] = {uint64_t(D), uint64_t(Nq), uint64_t(B) * H};
   const uint64_t sq[2] = {uint64_t(D) * 2, uint64_t(Nq) * D * 2};
@@ -1278,6 +1299,7 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   a.c_log2 = scale * kLog2e;
   a.scale = scale;
   a.causal = causal;
+  a.diag_wait_ns = 0;
 
   const long long rows = (long long)B * H * Nq;
   const long long threads = rows * (D / 8);
@@ -1292,6 +1314,7 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     a.launch_id = next_launch_id();
+    a.diag_wait_ns = diag_wait_ns;
     bwd_fused_kernel<<<grid_kv, 512, FusedCfg::kSmemBytes, stream>>>(tq64, tdo64, tk, tv, tdk, tdv,
                                                                      a, dq_acc);
     e = cudaGetLastError();
@@ -1316,6 +1339,7 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   a.launch_id = next_launch_id();
+  a.diag_wait_ns = diag_wait_ns;
   bwd_dkdv_kernel<D><<<grid_kv, 384, DkvCfg<D>::kSmemBytes, stream>>>(tq64, tdo64, tk, tv, tdk,
                                                                        tdv, a);
   return cudaGetLastError();
@@ -1335,8 +1359,8 @@ size_t backward_workspace_bytes(int B, int H, int Nq, int d, bool deterministic)
 cudaError_t backward_launch(const void* q, const void* k, const void* v, const void* o,
                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
                             int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
-                            bool deterministic, void* workspace, cudaStream_t stream,
-                            const char** err) {
+                            bool deterministic, unsigned diag_wait_ns, void* workspace,
+                            cudaStream_t stream, const char** err) {
   float* delta = static_cast<float*>(workspace);
   if (d == 128) {
     float* acc = nullptr;
@@ -1345,10 +1369,10 @@ cudaError_t backward_launch(const void* q, const void* k, const void* v, const v
       acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + (n + 255) / 256 * 256);
     }
     return launch_bwd<128>(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, Nq, Nk, scale, causal,
-                           delta, acc, stream, err);
+                           delta, acc, diag_wait_ns, stream, err);
   }
   return launch_bwd<64>(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, Nq, Nk, scale, causal, delta,
-                        nullptr, stream, err);
+                        nullptr, diag_wait_ns, stream, err);
 }
 
 int backward_take_device_error() {

@@ -188,8 +188,15 @@ def test_attn_bwd_ex_flags(lib):
     a = [_fake(i) for i in range(1, 10)]
     common = (1, 4, 2, 256, 256, 128, 0.088, 1, _fake(10), 1 << 20)
     # unknown flag bits are rejected before anything else happens
-    assert lib.attn_bwd_ex(*a, *common, 2, None) == binding.ATTN_EINVAL
-    assert "flags" in lib.attn_last_error().decode()
+    for bad in (0x4, 0x8, 0x80000000):
+        assert lib.attn_bwd_ex(*a, *common, bad, None) == binding.ATTN_EINVAL
+        assert "flags" in lib.attn_last_error().decode()
+    # the known flags pass the flag check (and fail later, on the fake
+    # workspace size, not on the flags)
+    for good in (binding.ATTN_BWD_DETERMINISTIC, binding.ATTN_BWD_DIAG_WAIT_EXPIRES):
+        tiny = (1, 4, 2, 256, 256, 128, 0.088, 1, _fake(10), 16)
+        assert lib.attn_bwd_ex(*a, *tiny, good, None) == binding.ATTN_EINVAL
+        assert "flags" not in lib.attn_last_error().decode()
     # the deterministic path needs only the D part of the workspace; the
     # default path at d = 128 needs the accumulator too
     small = (1, 4, 2, 256, 256, 128, 0.088, 1, _fake(10), 4096)
