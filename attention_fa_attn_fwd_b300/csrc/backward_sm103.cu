@@ -190,6 +190,9 @@ __global__ void __launch_bounds__(384, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  // Copies the producer has issued (for the abort drain at the end; kept in
+  // shared memory, not registers).
+  volatile int* issued_state = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
   const ErrSink err{g_backward_error, a.launch_id};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -209,6 +212,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < C::kNumBars; ++i)
       mbar_init(bar(i), (i == C::kBarQF || i == C::kBarPF || i == C::kBarPF + 1) ? 256u : 1u);
     *abort_flag = 0;
+    *issued_state = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -250,11 +254,7 @@ __global__ void __launch_bounds__(384, 1)
           tma_load_3d_elect(sbase + C::kOffV + vs * C::kTileBytes + s * C::kSlabBytes, &tm_v,
                             bar(C::kBarKF + ks), s * 64, j * 128, zkv);
         issued = j + 1;
-      }
-      if (!ok) {
-        const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
-        for (int j = max(0, issued - C::kKStages); j < issued; ++j)
-          mbar_wait_drain(bar(C::kBarKF + j % C::kKStages), (j / C::kKStages) & 1, deadline);
+        if (lane == 0) *issued_state = issued;
       }
     } else if (warp == 1 && n > 0) {
       // ------------------------------------------------------ MMA issuer
@@ -442,6 +442,16 @@ __global__ void __launch_bounds__(384, 1)
 
   tc_fence_before();
   __syncthreads();
+  // Abort path: every warp has stopped, so the flag is final.  Let every copy
+  // this CTA issued land before its shared memory is released (also the ones
+  // issued before another warp gave up).  Without an abort every copy has
+  // been consumed, and nothing waits here.
+  if (warp == 0 && *abort_flag) {
+    const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
+    const int issued = *issued_state;
+    for (int j = max(0, issued - C::kKStages); j < issued; ++j)
+      mbar_wait_drain(bar(C::kBarKF + j % C::kKStages), (j / C::kKStages) & 1, deadline);
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -494,6 +504,9 @@ __global__ void __launch_bounds__(384, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  // Copies the producer has issued (for the abort drain at the end; kept in
+  // shared memory, not registers).
+  volatile int* issued_state = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
   float* stat = reinterpret_cast<float*>(smem + C::kOffStat);
   const ErrSink err{g_backward_error, a.launch_id};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -525,6 +538,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(i), cnt);
     }
     *abort_flag = 0;
+    issued_state[0] = 0;  // Q / dO half-stages
+    issued_state[1] = 0;  // the K and V tiles
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -549,6 +564,7 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 0 && n_it > 0) {
       // ------------------------------------------------------ producer
       mbar_arrive_expect_tx_elect(bar(C::kBarKVF), 2 * C::kTileBytes);
+      if (lane == 0) issued_state[1] = 1;
       for (int s = 0; s < C::kSlabs; ++s) {
         tma_load_3d_elect(sbase + C::kOffK + s * C::kSlabBytes, &tm_k, bar(C::kBarKVF), s * 64, k0,
                           zkv);
@@ -592,12 +608,7 @@ __global__ void __launch_bounds__(384, 1)
                             bar(C::kBarQF + hs), s * 64, r0, hq);
         }
         issued = u + 1;
-      }
-      if (!ok) {
-        const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
-        mbar_wait_drain(bar(C::kBarKVF), 0, deadline);
-        for (int u = max(0, issued - C::kHS); u < issued; ++u)
-          mbar_wait_drain(bar(C::kBarQF + u % C::kHS), (u / C::kHS) & 1, deadline);
+        if (lane == 0) issued_state[0] = issued;
       }
     } else if (warp == 1 && n_it > 0) {
       // ------------------------------------------------------ MMA issuer
@@ -778,6 +789,18 @@ __global__ void __launch_bounds__(384, 1)
 
   tc_fence_before();
   __syncthreads();
+  // Abort path: every warp has stopped, so the flag is final.  Let every copy
+  // this CTA issued land before its shared memory is released (also the ones
+  // issued before another warp gave up).  Without an abort every copy has
+  // been consumed, and nothing waits here.
+  if (warp == 0 && *abort_flag) {
+    const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
+    const int issued = issued_state[0];
+    const bool issued_kv = issued_state[1] != 0;
+    if (issued_kv) mbar_wait_drain(bar(C::kBarKVF), 0, deadline);
+    for (int u = max(0, issued - C::kHS); u < issued; ++u)
+      mbar_wait_drain(bar(C::kBarQF + u % C::kHS), (u / C::kHS) & 1, deadline);
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -855,6 +878,9 @@ __global__ void __launch_bounds__(512, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  // Copies the producer has issued (for the abort drain at the end; kept in
+  // shared memory, not registers).
+  volatile int* issued_state = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
   float* stat = reinterpret_cast<float*>(smem + C::kOffStat);
   const ErrSink err{g_backward_error, a.launch_id};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -885,6 +911,8 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(bar(i), cnt);
     }
     *abort_flag = 0;
+    issued_state[0] = 0;  // Q / dO half-stages
+    issued_state[1] = 0;  // the K and V tiles
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -909,6 +937,7 @@ __global__ void __launch_bounds__(512, 1)
     if (warp == 0 && n_it > 0) {
       // ------------------------------------------------------ producer
       mbar_arrive_expect_tx_elect(bar(C::kBarKVF), 2 * C::kTileBytes);
+      if (lane == 0) issued_state[1] = 1;
       for (int s = 0; s < C::kSlabs; ++s) {
         tma_load_3d_elect(sbase + C::kOffK + s * C::kSlabBytes, &tm_k, bar(C::kBarKVF), s * 64, k0,
                           zkv);
@@ -965,13 +994,8 @@ __global__ void __launch_bounds__(512, 1)
                             bar(C::kBarQF + hs), s * 64, r0, hq);
         }
         issued = u + 1;
+        if (lane == 0) issued_state[0] = issued;
         load_stats(u + 1);
-      }
-      if (!ok) {
-        const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
-        mbar_wait_drain(bar(C::kBarKVF), 0, deadline);
-        for (int u = max(0, issued - C::kHS); u < issued; ++u)
-          mbar_wait_drain(bar(C::kBarQF + u % C::kHS), (u / C::kHS) & 1, deadline);
       }
     } else if ((warp == 1 || warp == 2) && n_it > 0) {
       // ---------------------------------------------- MMA issuers (two warps)
@@ -1225,6 +1249,18 @@ __global__ void __launch_bounds__(512, 1)
 
   tc_fence_before();
   __syncthreads();
+  // Abort path: every warp has stopped, so the flag is final.  Let every copy
+  // this CTA issued land before its shared memory is released (also the ones
+  // issued before another warp gave up).  Without an abort every copy has
+  // been consumed, and nothing waits here.
+  if (warp == 0 && *abort_flag) {
+    const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
+    const int issued = issued_state[0];
+    const bool issued_kv = issued_state[1] != 0;
+    if (issued_kv) mbar_wait_drain(bar(C::kBarKVF), 0, deadline);
+    for (int u = max(0, issued - C::kHS); u < issued; ++u)
+      mbar_wait_drain(bar(C::kBarQF + u % C::kHS), (u / C::kHS) & 1, deadline);
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();

@@ -160,6 +160,10 @@ __global__ void __launch_bounds__(384, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  // Copies the producer has issued, for the abort drain at the end (kept in
+  // shared memory, not registers): [0] V tiles (each with K_{j+1} on its
+  // barrier); [1] bit 0: K_0, bits 1-2: the Q tiles.
+  volatile int* issued_state = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
   const ErrSink err{g_prefill_error, a.launch_id};
 
   const int warp = threadIdx.x >> 5;
@@ -252,6 +256,10 @@ __global__ void __launch_bounds__(384, 1)
     if (lane < C::kNumBars)
       mbar_init(bar(lane), (lane >= C::kBarPF && lane < C::kBarPF2 + 2) ? 128u : 1u);
     if (lane == 0) *abort_flag = 0;
+    if (lane == 1) issued_state[0] = 0;
+    if (lane == 2)  // the Q tiles and (contiguous K) K_0 leave early
+      issued_state[1] = (n_kv > 0 && !kPaged ? 1 : 0) | (n_kv > 0 && n_t[0] > 0 ? 2 : 0) |
+                        (n_kv > 0 && n_t[1] > 0 ? 4 : 0);
     fence_mbar_init();
     __syncwarp();
   }
@@ -259,7 +267,7 @@ __global__ void __launch_bounds__(384, 1)
   // CTA-wide barrier below, from the thread that initialised the barriers, so
   // their latency overlaps the TMEM allocation and the rest of the set-up
   // (about 1.2 us per CTA, a large share of a short causal tile pair).
-  const bool early = n_kv > 0 && (a.diag_wait_ns == 0 || blockIdx.x != 0);
+  const bool early = n_kv > 0;
   if (warp == 0) {
     __syncwarp();
     if (early) {
@@ -302,19 +310,6 @@ __global__ void __launch_bounds__(384, 1)
         if (n_t[i] > 0) mbar_wait_drain(bar(C::kBarQF + i), 0, deadline);
       if (!kPaged) mbar_wait_drain(bar(C::kBarKF), 0, deadline);
     }
-    n_t[0] = n_t[1] = 0;
-    n_kv = 0;
-  }
-
-  // Failure-detection test (attn_fwd_ex with ATTN_FWD_DIAG_WAIT_EXPIRES): in
-  // CTA 0, before any copy or MMA is issued, one thread waits on a barrier
-  // nothing signals, with a short limit.  The wait expires and records a
-  // timeout for this launch; the CTA then does no work, and later CTAs of the
-  // same launch skip theirs.  Other launches are unaffected.
-  if (a.diag_wait_ns != 0 && blockIdx.x == 0) {
-    if (threadIdx.x == 0)
-      mbar_wait_limit(bar(C::kBarDiag), 0, abort_flag, err, kErrTimeoutDiag, a.diag_wait_ns);
-    __syncthreads();
     n_t[0] = n_t[1] = 0;
     n_kv = 0;
   }
@@ -395,9 +390,23 @@ __global__ void __launch_bounds__(384, 1)
             mbar_arrive_expect_tx_elect(bar(C::kBarKF), C::kTileBytes);
             load_tile(&tm_k, sbase + C::kOffK, bar(C::kBarKF), 0, prow);
             k0_issued = true;
+            if (lane == 0) issued_state[1] = issued_state[1] | 1;
           }
         }
+        // Failure-detection test (attn_fwd_ex with ATTN_FWD_DIAG_WAIT_EXPIRES):
+        // in CTA 0, two KV steps in, the producer waits on a barrier nothing
+        // signals, with a short limit, while copies and products of the CTA
+        // are in flight.  The wait expires and records a timeout for this
+        // launch; every warp of the CTA drains what it issued, and later CTAs
+        // of the launch skip their work.  Other launches are unaffected.
+        const int diag_j = (a.diag_wait_ns != 0 && blockIdx.x == 0) ? min(2, n_kv - 1) : -1;
         for (int j = 0; ok && j < n_kv; ++j) {
+          if (j == diag_j) {
+            __all_sync(0xffffffffu, mbar_wait_limit(bar(C::kBarDiag), 0, abort_flag, err,
+                                                    kErrTimeoutDiag, a.diag_wait_ns));
+            ok = false;
+            break;
+          }
           const int vs = j % C::kVStages;
           const bool next = j + 1 < n_kv;
           const int ks1 = (j + 1) % C::kKStages;
@@ -419,17 +428,9 @@ __global__ void __launch_bounds__(384, 1)
             load_tile(&tm_k, sbase + C::kOffK + ks1 * C::kTileBytes, bar(C::kBarVF + vs), j + 1,
                       prow_next);
           v_issued = j + 1;
+          if (lane == 0) issued_state[0] = v_issued;
           prow = prow_next;
           phys_next = phys_after;
-        }
-        if (!ok) {
-          // Abort path: let every copy already in flight land before exit.
-          const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
-          for (int i = 0; i < 2; ++i)
-            if (n_t[i] > 0) mbar_wait_drain(bar(C::kBarQF + i), 0, deadline);
-          if (k0_issued) mbar_wait_drain(bar(C::kBarKF), 0, deadline);
-          for (int j = max(0, v_issued - C::kVStages); j < v_issued; ++j)
-            mbar_wait_drain(bar(C::kBarVF + j % C::kVStages), (j / C::kVStages) & 1, deadline);
         }
       }
     } else if (warp == 1) {
@@ -712,6 +713,19 @@ __global__ void __launch_bounds__(384, 1)
 
   tc_fence_before();
   __syncthreads();
+  // Abort path: every warp has stopped, so the flag is final.  Let every copy
+  // this CTA issued land before its shared memory is released (also the ones
+  // issued before another warp gave up).  Without an abort every copy has
+  // been consumed, and nothing waits here.
+  if (warp == 0 && *abort_flag) {
+    const uint64_t deadline = globaltimer_ns() + kWaitTimeoutNs;
+    const int v_issued = issued_state[0], first = issued_state[1];
+    for (int i = 0; i < 2; ++i)
+      if (first & (2 << i)) mbar_wait_drain(bar(C::kBarQF + i), 0, deadline);
+    if (first & 1) mbar_wait_drain(bar(C::kBarKF), 0, deadline);
+    for (int j = max(0, v_issued - C::kVStages); j < v_issued; ++j)
+      mbar_wait_drain(bar(C::kBarVF + j % C::kVStages), (j / C::kVStages) & 1, deadline);
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();

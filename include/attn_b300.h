@@ -103,11 +103,12 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
 #define ATTN_FWD_EXP2_FMA 1u
 /*
  *   ATTN_FWD_DIAG_WAIT_EXPIRES  a failure-detection test, not for normal use
- *       (the source pages have no counterpart).  In the first CTA, before any
- *       copy or matrix product is issued, one bounded wait on a barrier that
- *       nothing signals expires after 1 ms.  The launch then records a timeout
- *       (code 0x105, read by attn_device_status) and its outputs are
- *       undefined.  It shows that an expired wait is survived and stays
+ *       (the source pages have no counterpart).  In the first CTA, two key
+ *       tiles in (copies and matrix products of the CTA in flight), one
+ *       bounded wait on a barrier that nothing signals expires after 1 ms;
+ *       every warp of that CTA drains what it issued and exits, later CTAs of
+ *       the launch skip their work.  The launch records a timeout (code
+ *       0x105, read by attn_device_status) and its outputs are undefined.  It shows that an expired wait is survived and stays
  *       confined to its own launch: later calls, and calls on other streams,
  *       compute normally without attn_device_status being called in between.
  */
