@@ -574,7 +574,18 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = true;
       int issued = 0;
       // Half u = 2*it + h: queries h*64 .. h*64+63 of (query head, tile) it.
+      // Failure-detection test (ATTN_BWD_DIAG_WAIT_EXPIRES): in CTA 0, a few
+      // query halves in, the producer waits on a barrier nothing signals,
+      // with a short limit, while copies and products of the CTA are in
+      // flight; the wait expires and every warp of the CTA drains.
+      const int diag_u = (a.diag_wait_ns != 0 && blockIdx.x == 0) ? min(4, 2 * n_it - 1) : -1;
       for (int u = 0; u < 2 * n_it; ++u) {
+        if (u == diag_u) {
+          __all_sync(0xffffffffu, mbar_wait_limit(bar(C::kBarDiag), 0, abort_flag, err,
+                                                  kErrTimeoutDiag, a.diag_wait_ns));
+          ok = false;
+          break;
+        }
         const int it = u >> 1, h = u & 1;
         const int hs = u % C::kHS;
         const int hq = b * a.H + g * G + it / per_head;  // query (b, h) row of the tensor maps
@@ -648,14 +659,6 @@ __global__ void __launch_bounds__(384, 1)
       // dV += P^T_h dO[h], dK += dS^T_h Q[h] (16 queries per MMA); frees the half-stage.
       auto issue_acc = [&](int u) -> bool {
         const int h = u & 1, hs = u % C::kHS;
-        // Failure-detection test (ATTN_BWD_DIAG_WAIT_EXPIRES): in CTA 0, a
-        // few halves in, a wait on a barrier nothing signals expires, with
-        // copies and products still in flight; every warp then drains.
-        if (a.diag_wait_ns != 0 && blockIdx.x == 0 && u == min(3, 2 * n_it - 1)) {
-          __all_sync(0xffffffffu, mbar_wait_limit(bar(C::kBarDiag), 0, abort_flag, err,
-                                                  kErrTimeoutDiag, a.diag_wait_ns));
-          return false;
-        }
         if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kBarPF + h), (u >> 1) & 1, abort_flag, err,
                                                kErrTimeoutMma)))
           return false;
@@ -966,7 +969,18 @@ __global__ void __launch_bounds__(512, 1)
         }
       };
       load_stats(0);
+      // Failure-detection test (ATTN_BWD_DIAG_WAIT_EXPIRES): in CTA 0, a few
+      // query halves in, the producer waits on a barrier nothing signals,
+      // with a short limit, while copies and products of the CTA are in
+      // flight; the wait expires and every warp of the CTA drains.
+      const int diag_u = (a.diag_wait_ns != 0 && blockIdx.x == 0) ? min(4, 2 * n_it - 1) : -1;
       for (int u = 0; u < 2 * n_it; ++u) {
+        if (u == diag_u) {
+          __all_sync(0xffffffffu, mbar_wait_limit(bar(C::kBarDiag), 0, abort_flag, err,
+                                                  kErrTimeoutDiag, a.diag_wait_ns));
+          ok = false;
+          break;
+        }
         const int it = u >> 1, h = u & 1;
         const int hs = u % C::kHS;
         const int hq = b * a.H + g * G + it / per_head;
@@ -1065,15 +1079,6 @@ __global__ void __launch_bounds__(512, 1)
         const uint64_t ds_desc = smem_desc_sw128(sbase + C::kOffDS, C::kDSBytes, 1024);
         for (int u = 0; ok && u < n_u; ++u) {
           const int h = u & 1, hs = u % C::kHS;
-          // Failure-detection test (ATTN_BWD_DIAG_WAIT_EXPIRES): in CTA 0, a
-          // few halves in, a wait on a barrier nothing signals expires, with
-          // copies and products still in flight; every warp then drains.
-          if (a.diag_wait_ns != 0 && blockIdx.x == 0 && u == min(3, n_u - 1)) {
-            __all_sync(0xffffffffu, mbar_wait_limit(bar(C::kBarDiag), 0, abort_flag, err,
-                                                    kErrTimeoutDiag, a.diag_wait_ns));
-            ok = false;
-            break;
-          }
           ok = wait_on(C::kBarPF + h, (u >> 1) & 1);  // P^T, dS^T of half u written
           if (!ok) break;
           // dV += P^T_h dO[u], dK += dS^T_h Q[u]; then the half-stage and

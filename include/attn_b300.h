@@ -215,10 +215,10 @@ ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const
  *       of five, so it is slower).  Needs only the D part of the workspace
  *       (B*H*Nq floats rounded up to 256 bytes).
  *   ATTN_BWD_DIAG_WAIT_EXPIRES  a failure-detection test, not for normal use:
- *       in the first CTA of the key-stationary kernel, the warp that issues
- *       the dV / dK products lets one bounded wait (on a barrier nothing
- *       signals, 1 ms limit) expire after a few query halves, with copies and
- *       products of the CTA still in flight.  Every warp of that CTA then
+ *       in the first CTA of the key-stationary kernel, the producer warp lets
+ *       one bounded wait (on a barrier nothing signals, 1 ms limit) expire a
+ *       few query halves in, with copies and products of the CTA still in
+ *       flight.  Every warp of that CTA then
  *       drains what it issued and exits; later CTAs of the launch skip their
  *       work.  The outputs of this call are undefined; attn_device_status
  *       reports code 0x105 once; later calls are unaffected.
