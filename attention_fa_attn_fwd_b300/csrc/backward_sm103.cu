@@ -10,9 +10,14 @@
 //   dQ = scale dS K,  dK = scale dS^T Q,
 // and a KV head's gradient sums over the query heads that read it (GQA).
 //
-// Three kernels, all on the caller's stream, no atomics (deterministic):
-//   bwd_delta_kernel   D = rowsum(dO o O) in fp32 (bandwidth-bound) into the
-//                      workspace.
+// Two paths, all kernels on the caller's stream:
+//   default at d = 128:  bwd_delta_kernel (D = rowsum(dO o O), and zeroes an
+//                      fp32 dQ accumulator) + bwd_fused_kernel (key-
+//                      stationary, all five products; dQ summed over key
+//                      tiles with fp32 atomic adds, see its own comment) +
+//                      bwd_dq_convert_kernel (dq = bf16(scale * acc)).
+//   ATTN_BWD_DETERMINISTIC, and d = 64, no atomics (bit-reproducible):
+//   bwd_delta_kernel   D into the workspace (bandwidth-bound).
 //   bwd_dq_kernel      Q-stationary: a CTA owns 128 query rows of one head and
 //                      streams the K/V tiles they attend: S = Q K^T and
 //                      dP = dO V^T into TMEM, dS (bf16) back into TMEM,
@@ -20,18 +25,18 @@
 //   bwd_dkdv_kernel    KV-stationary: a CTA owns 128 keys of one KV head and
 //                      streams, for every query head of its group, the Q/dO
 //                      tiles that attend them (in half-tiles of 64 queries,
-//                      each released as soon as its products are issued): S^T = K Q^T and dP^T = V dO^T,
-//                      P^T and dS^T (bf16) back into TMEM, dV += P^T dO and
-//                      dK += dS^T Q accumulated in TMEM.
-// Splitting dQ from dK/dV recomputes S and dP once more (7 instead of 5
-// matrix products) but keeps every accumulator in TMEM (dQ would need a
-// fifth 128-column TMEM block or fp32 atomics in the KV-stationary kernel).
+//                      each released as soon as its products are done):
+//                      S^T = K Q^T and dP^T = V dO^T, P^T and dS^T (bf16)
+//                      back into TMEM, dV += P^T dO and dK += dS^T Q
+//                      accumulated in TMEM.
+//   Splitting dQ from dK/dV recomputes S and dP once more (7 instead of 5
+//   matrix products) but keeps every accumulator in TMEM.
 //
-// Warp roles in both tcgen05 kernels (12 warps): warp 0 TMA producer, warp 1
-// MMA issuer (one elected lane), warps 2-3 idle, warps 4-7 and 8-11 two
-// compute warpgroups.  Every 128-wide score tile is split into two 64-wide
-// halves, one per compute warpgroup, each with its own TMEM buffer (S and dP
-// side by side, 64 columns each).  The MMA warp issues the next tile's
+// Warp roles in the two deterministic tcgen05 kernels (12 warps): warp 0 TMA
+// producer, warp 1 MMA issuer (one elected lane), warps 2-3 idle, warps 4-7
+// and 8-11 two compute warpgroups.  Every 128-wide score tile is split into
+// two 64-wide halves, one per compute warpgroup, each with its own TMEM
+// buffer (S and dP side by side, 64 columns each).  The MMA warp issues the next tile's
 // products for one half while the other half's warpgroup is still computing,
 // and the accumulating products (dQ, or dV and dK) of a half as soon as its
 // warpgroup has written its bf16 operands, so the tensor pipe and the
@@ -817,9 +822,11 @@ __global__ void __launch_bounds__(384, 1)
 // tile) that sees them, as bwd_dkdv_kernel does, and also forms this key
 // tile's share of dQ:
 //   dQ^T_u = K^T dS^T_u   (M = d = 128, N = 64 queries, K = 128 keys)
-// from the bf16 dS^T the compute warpgroup writes to shared memory.  dQ^T
-// lands in the half's dP^T columns of TMEM (free once the compute
-// warpgroup has read them); a fourth warpgroup reads it out (lane = d, so a
+// from the bf16 dS^T the compute warpgroup writes to shared memory (P^T and
+// dS^T also go back to TMEM, over the S^T columns they came from, as the A
+// operands of dV and dK).  dQ^T lands in the half's dP^T columns of TMEM
+// (free once the compute warpgroup has read them); a fourth warpgroup reads
+// it out (lane = d, so a
 // warp's 32 lanes cover 32 consecutive floats of one query row) and adds it
 // to an fp32 dQ accumulator in the workspace with coalesced atomic adds in
 // L2.  A conversion kernel then writes dq = bf16(scale * accumulator).  The
