@@ -47,7 +47,8 @@ def _case(seed):
 
 def test_a_timeout_stays_inside_its_launch():
     """attn_fwd_ex(ATTN_FWD_DIAG_WAIT_EXPIRES) lets one bounded wait of a real
-    prefill launch expire (CTA 0, before any copy or product is issued).
+    prefill launch expire (CTA 0, in the producer two key tiles in, with
+    copies and products of the CTA in flight, which its warps drain).
     The next launch, with no attn_device_status in between, must compute the
     right result: the timeout skips work only in the launch that recorded
     it.  attn_device_status then reports the code once."""
