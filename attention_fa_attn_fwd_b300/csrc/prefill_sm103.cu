@@ -569,32 +569,40 @@ __global__ void __launch_bounds__(384, 1)
       if (!ok) break;
       tc_fence_after();
       uint32_t s[128];
-      tmem_ld32(lane_base + col_s + 0, s + 0);
-      tmem_ld32(lane_base + col_s + 32, s + 32);
-      tmem_ld32(lane_base + col_s + 64, s + 64);
-      tmem_ld32(lane_base + col_s + 96, s + 96);
+      // Each load also returns the maximum of its 32 columns (sm_103a).
+      float cm[4];
+      tmem_ld32_max(lane_base + col_s + 0, s + 0, cm[0]);
+      tmem_ld32_max(lane_base + col_s + 32, s + 32, cm[1]);
+      tmem_ld32_max(lane_base + col_s + 64, s + 64, cm[2]);
+      tmem_ld32_max(lane_base + col_s + 96, s + 96, cm[3]);
       tmem_ld_wait();
       reg_fence<128>(s);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) asm volatile("" : "+f"(cm[i]));
 
       const int lim = row_last - j * 128;  // columns > lim are masked
+      float rmax;
       if (lim < 127) {
+        // diagonal or tail tile: mask first, then the maximum of what is left
 #pragma unroll
         for (int cc = 0; cc < 128; ++cc)
           if (cc > lim) s[cc] = __float_as_uint(-INFINITY);
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i]);
+#pragma unroll
+        for (int cc = 8; cc < 120; cc += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            mx[i] = max3f(mx[i], __uint_as_float(s[cc + i]), __uint_as_float(s[cc + 8 + i]));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(s[120 + i]));
+        rmax = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+      } else {
+        rmax = fmaxf(max3f(cm[0], cm[1], cm[2]), cm[3]);
       }
       __syncwarp();
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i]);
-#pragma unroll
-      for (int cc = 8; cc < 120; cc += 16)
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          mx[i] = max3f(mx[i], __uint_as_float(s[cc + i]), __uint_as_float(s[cc + 8 + i]));
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(s[120 + i]));
-      const float mt =
-          max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c;
+      const float mt = rmax * c;
       // Move the reference only when the max grew by more than the threshold
       // (or on the first finite max).  alpha rescales l and O.
       const bool move = mt > m + kRescaleThreshold;

@@ -340,6 +340,33 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
+// tmem_ld32 that also returns, per thread, the maximum of the 32 values it
+// loads (tcgen05.ld.red, sm_103a).  Issue only, like tmem_ld32: both are
+// valid after tmem_ld_wait() + reg_fence().
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t* r, float& mx) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+      : "=f"(*reinterpret_cast<float*>(&r[0])), "=f"(*reinterpret_cast<float*>(&r[1])),
+        "=f"(*reinterpret_cast<float*>(&r[2])), "=f"(*reinterpret_cast<float*>(&r[3])),
+        "=f"(*reinterpret_cast<float*>(&r[4])), "=f"(*reinterpret_cast<float*>(&r[5])),
+        "=f"(*reinterpret_cast<float*>(&r[6])), "=f"(*reinterpret_cast<float*>(&r[7])),
+        "=f"(*reinterpret_cast<float*>(&r[8])), "=f"(*reinterpret_cast<float*>(&r[9])),
+        "=f"(*reinterpret_cast<float*>(&r[10])), "=f"(*reinterpret_cast<float*>(&r[11])),
+        "=f"(*reinterpret_cast<float*>(&r[12])), "=f"(*reinterpret_cast<float*>(&r[13])),
+        "=f"(*reinterpret_cast<float*>(&r[14])), "=f"(*reinterpret_cast<float*>(&r[15])),
+        "=f"(*reinterpret_cast<float*>(&r[16])), "=f"(*reinterpret_cast<float*>(&r[17])),
+        "=f"(*reinterpret_cast<float*>(&r[18])), "=f"(*reinterpret_cast<float*>(&r[19])),
+        "=f"(*reinterpret_cast<float*>(&r[20])), "=f"(*reinterpret_cast<float*>(&r[21])),
+        "=f"(*reinterpret_cast<float*>(&r[22])), "=f"(*reinterpret_cast<float*>(&r[23])),
+        "=f"(*reinterpret_cast<float*>(&r[24])), "=f"(*reinterpret_cast<float*>(&r[25])),
+        "=f"(*reinterpret_cast<float*>(&r[26])), "=f"(*reinterpret_cast<float*>(&r[27])),
+        "=f"(*reinterpret_cast<float*>(&r[28])), "=f"(*reinterpret_cast<float*>(&r[29])),
+        "=f"(*reinterpret_cast<float*>(&r[30])), "=f"(*reinterpret_cast<float*>(&r[31])),
+        "=f"(mx)
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
